@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark of the paged GQA/MQA attention step on GB300.
+
+One step = the whole hot path over one batch: reshape_and_cache of the
+step's new K/V rows into the paged cache, then paged attention (decode, or
+the mixed chunked-prefill + decode batch), all through the C ABI.
+
+Headline workload (one GPU): Llama-3.1-8B-shaped decode -- 256 sequences,
+32 query / 8 KV heads, head_dim 128, bf16, block 16, lognormal context
+lengths (median 400, clipped to [16, 4096]).  Metric: KV-cache GB/s, the
+algorithmic bytes sum_b ctx_b * Hkv * D * 2 (K and V) * 2 bytes over the
+step time.  The mixed batch (64 sequences: 16 query chunks + 48 decode rows)
+is reported beside it in tokens/s.
+
+Inputs are synthetic and seeded (workloads/); under torchrun every rank runs
+its own replica (the path has no exchange step), so scaling is weak.
+
+--impl reference times the fp64 CPU oracle, as it stands, on the host cores
+(a bounded sample of the same workload per step); it is the slow reference
+arm of this benchmark, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged GQA decode KV-cache GB/s (% of GB300 HBM peak); mixed-batch tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_decode",
+                    choices=["llama8b_decode", "mixed_prefill_decode", "head_sweep_kv1",
+                             "head_sweep_kv8", "head_sweep_kv32", "long_context_decode",
+                             "tiny_gqa_decode"])
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the mixed-batch line item")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def make_workload(name: str, seed: int):
+    if name.startswith("head_sweep_kv"):
+        return W.head_sweep(seed, num_kv_heads=int(name[len("head_sweep_kv"):]))
+    return W.CONFIGS[name](seed)
+
+
+# ---------------------------------------------------------------- env helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clk", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[1]) for r in rows]
+        smax = max(num(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": float(np.nanmedian(sm)), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(num(r[3]) for r in rows)}
+
+
+def kernel_source_sha(fname: str) -> str:
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "mqa_paged_kv_gb300", "csrc", fname), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str, src_file: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/), or None
+    when no capture matches the current kernel source and workload."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha(src_file)
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+            if (parts.get("kernel") == kernel_key and parts.get("source_sha") == sha
+                    and parts.get("workload") == workload):
+                try:
+                    return float(parts["bytes_per_launch"])
+                except (KeyError, ValueError):
+                    return None
+    return None
+
+
+# ---------------------------------------------------------------- CPU arms
+def oracle_sample_rows(case, target_s: float, threads: int):
+    """Pick a prefix of query rows whose oracle run takes about target_s."""
+    import oracle
+    T = case.total_query_tokens
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+    rng = np.random.default_rng(1234)
+    order = rng.permutation(T)
+    n = max(1, min(T, 8))
+    while True:
+        rows = np.sort(order[:n])
+        t0 = time.perf_counter()
+        oracle.paged_attention(case.q, kc, vc, case.block_tables, case.cu_query_lens,
+                               case.context_lens, case.scale, case.num_kv_heads, case.dtype,
+                               rows=rows, num_threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or n >= T:
+            break
+        n = min(T, int(n * max(2.0, target_s / max(dt, 1e-3))))
+    return rows, kc, vc
+
+
+def sample_kv_bytes(case, rows):
+    """KV bytes the attention of `rows` reads (each row's visible keys, once
+    per KV head), the same algorithmic count as the GPU metric."""
+    cu = case.cu_query_lens
+    b_of = np.searchsorted(cu, rows, side="right") - 1
+    ctx = case.context_lens[b_of].astype(np.int64)
+    ql = (cu[b_of + 1] - cu[b_of]).astype(np.int64)
+    pos = ctx - ql + (rows - cu[b_of])
+    if case.is_decode:
+        keys = ctx
+    else:
+        keys = pos + 1
+    return int(keys.sum()) * case.num_kv_heads * case.head_dim * 2 * case.elem_bytes
+
+
+def run_oracle_timed(case, rows, kc, vc, threads, reps=1):
+    import oracle
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.paged_attention(case.q, kc, vc, case.block_tables, case.cu_query_lens,
+                               case.context_lens, case.scale, case.num_kv_heads, case.dtype,
+                               rows=rows, num_threads=threads)
+    return (time.perf_counter() - t0) / reps
+
+
+def cpu_baseline(case, target_s=12.0):
+    import oracle
+    threads = os.cpu_count() or 1
+    rows, kc, vc = oracle_sample_rows(case, target_s / 3, threads)
+    dt = run_oracle_timed(case, rows, kc, vc, threads)
+    kvb = sample_kv_bytes(case, rows)
+    return {"value": kvb / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} of {case.total_query_tokens} query rows of {case.name} "
+                      f"(all heads), {dt:.2f} s, fp64 OpenMP C"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    case = make_workload(args.workload, args.seed)
+    threads = os.cpu_count() or 1
+    rows, kc, vc = oracle_sample_rows(case, 2.0, threads)
+    kvb = sample_kv_bytes(case, rows)
+    for _ in range(args.warmup):
+        run_oracle_timed(case, rows, kc, vc, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_timed(case, rows, kc, vc, threads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = kvb / dt / 1e9
+    sample = (f"{len(rows)} of {case.total_query_tokens} query rows of {case.name} per step "
+              f"(all heads), fp64 OpenMP C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(W.describe(case), l2="n/a (host)", parallelism="rank 0 only"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+class Step:
+    """Device-resident inputs of one workload and its step through the C ABI."""
+
+    def __init__(self, case, device, splits):
+        import torch
+        import mqa_paged_kv_gb300 as pa
+        self.torch, self.pa, self.case, self.splits = torch, pa, case, splits
+        et = torch.float16 if case.dtype == W.F16 else torch.bfloat16
+        self.et = et
+
+        def dev(a, dt=None):
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            if a.dtype == np.uint16:
+                t = t.view(torch.int16).view(dt)
+            return t.to(device)
+
+        self.dev = dev
+        self.k_cache = dev(case.k_cache, et)
+        self.v_cache = dev(case.v_cache, et)
+        self.inputs = {
+            "q": dev(case.q, et), "k_new": dev(case.k_new, et), "v_new": dev(case.v_new, et),
+            "slot_mapping": dev(case.slot_mapping), "block_tables": dev(case.block_tables),
+            "context_lens": dev(case.context_lens), "cu_query_lens": dev(case.cu_query_lens),
+        }
+        self.out = torch.empty_like(self.inputs["q"])
+        if case.is_decode:
+            nb = pa.paged_attn_workspace_bytes(case.num_seqs, case.num_heads,
+                                               case.num_kv_heads, case.head_dim,
+                                               case.max_blocks_per_seq, case.block_size, splits)
+        else:
+            nb = pa.paged_attn_chunked_prefill_workspace_bytes(
+                case.num_seqs, case.total_query_tokens, case.num_heads, case.num_kv_heads,
+                case.head_dim, case.max_blocks_per_seq, case.block_size, splits)
+        self.ws = pa.alloc_workspace(nb, device)
+        self.launches = 0
+
+    def run(self, x=None, prof=None):
+        pa, c = self.pa, self.case
+        x = x or self.inputs
+        pa.reshape_and_cache(x["k_new"], x["v_new"], self.k_cache, self.v_cache,
+                             x["slot_mapping"])
+        n = pa.last_launch_count()
+        if prof is not None:
+            pa.pa_profile_next_call(*prof)
+        if c.is_decode:
+            pa.paged_attn_decode(x["q"], self.k_cache, self.v_cache, x["block_tables"],
+                                 x["context_lens"], c.scale, out=self.out,
+                                 num_splits=self.splits, workspace=self.ws)
+        else:
+            pa.paged_attn_chunked_prefill(x["q"], self.k_cache, self.v_cache, x["block_tables"],
+                                          x["cu_query_lens"], x["context_lens"],
+                                          c.max_query_len, c.scale, out=self.out,
+                                          num_splits=self.splits, workspace=self.ws)
+        n += pa.last_launch_count()
+        self.launches += n
+        return self.out
+
+
+def time_steps(step, steps, warmup, flush, e2e=False):
+    """Per-step CUDA-event times (ms) of the step and of its attention kernels;
+    L2 is flushed before every timed step, outside the timed interval."""
+    torch = step.torch
+    stream = torch.cuda.current_stream()
+    host = dev_bufs = None
+    if e2e:
+        host = {k: v.cpu().pin_memory() for k, v in step.inputs.items()}
+        dev_bufs = {k: torch.empty_like(v) for k, v in step.inputs.items()}
+        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+
+    def one(prof=None):
+        if e2e:
+            for k in host:
+                dev_bufs[k].copy_(host[k], non_blocking=True)
+            o = step.run(dev_bufs, prof)
+            out_host.copy_(o, non_blocking=True)
+        else:
+            step.run(None, prof)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    step.launches = 0
+    for i in range(steps):
+        flush.zero_()
+        e0, e1, k0, k1 = ev[i]
+        e0.record(stream)
+        one((k0, k1))
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = np.array([a.elapsed_time(b) for a, b, _, _ in ev])
+    kt = np.array([c.elapsed_time(d) for _, _, c, d in ev])
+    h2d = sum(v.numel() * v.element_size() for v in step.inputs.values()) if e2e else 0
+    d2h = step.out.numel() * step.out.element_size() if e2e else 0
+    return t, kt, h2d, d2h
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    import mqa_paged_kv_gb300  # noqa: F401  (fails loudly when the library is missing)
+
+    case = make_workload(args.workload, args.seed + rank)
+    step = Step(case, device, args.splits)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    clk = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk.start()
+    wall0 = time.perf_counter()
+    t, kt, _, _ = time_steps(step, args.steps, args.warmup, flush)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = clk.stop()
+    launches = step.launches
+
+    te, _, h2d, d2h = time_steps(step, max(3, args.steps // 2), 2, flush, e2e=True)
+
+    step_s = float(t.mean()) / 1e3
+    kern_s = float(kt.mean()) / 1e3
+    e2e_s = float(te.mean()) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        v = torch.tensor([step_s, e2e_s], device=device, dtype=torch.float64)
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        step_s, e2e_s = float(v[0]), float(v[1])
+
+    kvb = case.kv_bytes()
+    units = "GB/s"
+    value = kvb * world / step_s / 1e9
+    peak, peak_src = measured_hbm_peak()
+    achieved = kvb / kern_s / 1e9
+    main_kernel = "decode_kernel" if case.is_decode else "prefill_kernel+decode_kernel"
+    traffic = ncu_traffic("decode_kernel" if case.is_decode else "prefill_kernel",
+                          "decode.cu" if case.is_decode else "prefill.cu", case.name)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": units, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if case.dtype == W.BF16 else "f16", "data": "synthetic",
+        "config": dict(W.describe(case), splits=args.splits or "auto",
+                       l2=f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       step="reshape_and_cache + paged attention"),
+        "hbm_peak_frac": value / world / peak,
+        "tokens_per_s": case.total_query_tokens * world / step_s,
+        "roofline": {"bound": "hbm", "kernel": main_kernel, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": kvb,
+                     "traffic": traffic},
+        "e2e": {"value": kvb * world / e2e_s / 1e9, "unit": units, "ms_per_step": e2e_s * 1e3,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+
+    if not args.no_secondary and args.workload == "llama8b_decode":
+        mcase = W.mixed_prefill_decode(args.seed + rank)
+        mstep = Step(mcase, device, args.splits)
+        mt, mkt, _, _ = time_steps(mstep, max(5, args.steps // 2), 3, flush)
+        ms = float(mt.mean()) / 1e3
+        line["secondary"] = {"mixed_prefill_decode": {
+            "tokens_per_s": mcase.total_query_tokens / ms, "ms_per_step": ms * 1e3,
+            "attention_kernels_ms": float(mkt.mean()),
+            "kv_gbs": mcase.kv_bytes() / ms / 1e9, "query_tokens": mcase.total_query_tokens}}
+        del mstep
+
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline(case)
+        except Exception as e:  # the baseline is reported, never required
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:200]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) paged-KV GQA/MQA attention
+ * library (libpaged_attn.so).
+ *
+ * What is computed.  Attention of query heads over a paged KV cache, for
+ * grouped-query (G = num_heads / num_kv_heads query heads share one KV head)
+ * and multi-query (one KV head) models:
+ *
+ *   out[t, h, :] = sum_j softmax_j(scale * q[t, h, :] . K[j, h / G, :]) V[j, h / G, :]
+ *
+ * over the keys j that query token t may see.  This is exactly multi-head
+ * attention after each KV head is expanded to its G query heads, as in vLLM
+ * issue #1880 "[Performance] Use optimized kernels for MQA/GQA" (item 1); the
+ * kernels reach it without expanding, reading each KV head's cache blocks
+ * once for all G query heads and doing the grouped dot products on tensor
+ * cores (same issue, opening paragraph and item 2).  The mixed batch of
+ * chunked prefill and decode follows vLLM PR #14431 "[Kernel][V1] Further
+ * optimizations to ROCm (Triton) Backend to better handle GQA" (opening post,
+ * review thread on chunked_prefill_paged_decode).
+ *
+ * Data layout (all row-major, contiguous, element type fp16 or bf16):
+ *   q           [T, Hq, D]          (decode: T = num_seqs, one token each)
+ *   k_cache     [NB, Hkv, bs, D]    physical block, KV head, slot, dim
+ *   v_cache     [NB, Hkv, bs, D]
+ *   block_tables[B, max_blocks_per_seq] int32 physical block ids; entries
+ *               past a sequence's last block are not read (pad with -1)
+ *   context_lens[B] int32: tokens of each sequence in the cache, INCLUDING
+ *               this step's query tokens (written by reshape_and_cache first)
+ *   cu_query_lens[B + 1] int32: prefix sums of the query-token counts
+ *   out         [T, Hq, D], same element type as q
+ * Causal alignment: query token i of a sequence with qlen query tokens and
+ * ctx context tokens sits at position ctx - qlen + i and sees keys 0 .. that
+ * position.  A sequence with ctx = 0 gets a zero output row.
+ *
+ * Ownership and execution.  Every pointer argument is device memory owned
+ * by the caller (except where a function says "host").  Calls only enqueue
+ * work on `stream`; they never synchronise, never allocate device memory and
+ * never create streams.  Scratch space comes from the caller's `workspace`
+ * (size from the matching *_workspace_bytes function, 256-byte aligned).
+ * Two calls that share a workspace must not run concurrently.
+ *
+ * Errors.  Arguments are validated on the host first; a negative pa_status
+ * is returned and nothing is enqueued.  A failed launch returns
+ * PA_ERR_CUDA.  Data errors found on the device (a block id or a slot out of
+ * range, a pipeline wait that timed out) skip the faulty access and set bits
+ * in a status word inside the workspace, read with pa_read_device_status().
+ * The library never aborts, exits or traps.
+ */
+#ifndef PAGED_ATTN_H
+#define PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,       /* a required pointer is NULL */
+    PA_ERR_SHAPE = -2,      /* inconsistent or out-of-range sizes */
+    PA_ERR_DTYPE = -3,      /* element type is neither PA_F16 nor PA_BF16 */
+    PA_ERR_HEADDIM = -4,    /* head_dim not 64 or 128 */
+    PA_ERR_BLOCKSIZE = -5,  /* block_size not a multiple of 16 in [16, 256] */
+    PA_ERR_WORKSPACE = -6,  /* workspace NULL, too small or misaligned */
+    PA_ERR_CUDA = -7,       /* a CUDA runtime call or launch failed */
+    PA_ERR_ALIGN = -8,      /* a tensor pointer is not 16-byte aligned */
+    PA_ERR_DEVICE = -9      /* the current device is not sm_100-family */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the device status word (pa_read_device_status). */
+#define PA_DEV_BAD_BLOCK_ID 0x1u  /* a block-table entry outside [0, NB) */
+#define PA_DEV_BAD_SLOT 0x2u      /* a slot_mapping entry outside [-1, NB*bs) */
+#define PA_DEV_WAIT_TIMEOUT 0x4u  /* a pipeline wait ran out of time */
+#define PA_DEV_BAD_LENGTHS 0x8u   /* a sequence with ctx < 0, ctx > mbs * bs,
+                                     qlen < 0 or qlen > ctx: skipped */
+
+/* Human-readable name of a pa_status value (static string). */
+PA_API const char* pa_status_string(int status);
+
+/*
+ * reshape_and_cache -- write this step's new K/V rows into the paged cache.
+ *
+ *   k_cache[s / bs, h, s % bs, :] = k[t, h, :]   (same for v)
+ *   for every token t with s = slot_mapping[t] >= 0; slot -1 skips a token.
+ *
+ * Source: the cache-write step that precedes paged attention in the
+ * attention layer of the pages' serving system (vLLM issue #1880, item 2:
+ * the decode kernel reads K/V from the paged cache); layout as above.
+ *   k, v          [num_tokens, num_kv_heads, head_dim]
+ *   slot_mapping  [num_tokens] int64
+ * Every other byte of the caches is left unchanged.  Two tokens mapped to
+ * the same slot is invalid input (which one lands is unspecified).  A slot
+ * outside [-1, num_blocks * block_size) is skipped and flags
+ * PA_DEV_BAD_SLOT in `status_word` (a device int32, may be NULL).
+ */
+PA_API int reshape_and_cache(const void* k, const void* v, void* k_cache,
+                      void* v_cache, const int64_t* slot_mapping,
+                      int num_tokens, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, int dtype,
+                      uint32_t* status_word, pa_stream_t stream);
+
+/*
+ * Workspace size in bytes for paged_attn_decode with these sizes.
+ * num_splits: 0 = automatic (splits of 256 tokens, at most 64 per
+ * sequence), else the fixed number of KV splits per sequence (1..64).
+ */
+PA_API size_t paged_attn_workspace_bytes(int num_seqs, int num_heads,
+                                  int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int block_size,
+                                  int num_splits);
+
+/*
+ * paged_attn_decode -- one query token per sequence.
+ *
+ *   q [num_seqs, num_heads, head_dim]; out [num_seqs, num_heads, head_dim]
+ *
+ * Long contexts are cut into KV splits (split s of a sequence with nb
+ * blocks covers blocks [s * c, (s + 1) * c), c = ceil(nb / S)); each split
+ * gives a partial output and its log-sum-exp, merged by a log-sum-exp
+ * combine.  num_splits = 0 picks S per sequence (256-token splits, at most
+ * 64).  scale multiplies q . k before the softmax (base e).
+ */
+PA_API int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, float scale, int num_seqs,
+                      int num_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, int dtype,
+                      int num_splits, void* out, void* workspace,
+                      size_t workspace_bytes, pa_stream_t stream);
+
+/* Workspace size in bytes for paged_attn_chunked_prefill. */
+PA_API size_t paged_attn_chunked_prefill_workspace_bytes(
+    int num_seqs, int total_query_tokens, int num_heads, int num_kv_heads,
+    int head_dim, int max_blocks_per_seq, int block_size, int num_splits);
+
+/*
+ * paged_attn_chunked_prefill -- a batch mixing query chunks (qlen > 1,
+ * causal within the chunk, after a cached prefix) with decode rows
+ * (qlen = 1), in the cu_query_lens layout.
+ *
+ *   q [total_query_tokens, num_heads, head_dim]; out same shape.
+ *   total_query_tokens = cu_query_lens[num_seqs] and max_query_len are the
+ *   host-known bounds the launch is sized by (no device sync); rows of
+ *   sequences with qlen = 1 follow the decode path (with KV splits as in
+ *   paged_attn_decode), the rest the prefill path.
+ */
+PA_API int paged_attn_chunked_prefill(const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int max_blocks_per_seq,
+                               const int32_t* cu_query_lens,
+                               const int32_t* context_lens,
+                               int total_query_tokens, int max_query_len,
+                               float scale, int num_seqs, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, int dtype, int num_splits,
+                               void* out, void* workspace,
+                               size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Read (and clear, if `clear` != 0) the device status word kept in a
+ * workspace after the work queued on `stream` so far has finished.  This
+ * call synchronises `stream`.  *flags receives PA_DEV_* bits (host pointer).
+ */
+PA_API int pa_read_device_status(const void* workspace, int clear, uint32_t* flags,
+                          pa_stream_t stream);
+
+/*
+ * Measurement hook.  The next attention call made on this thread records
+ * `start_event` on its stream just before its first attention kernel
+ * (prefill or decode) and `stop_event` just after its last one, so the
+ * work-list build and the split combine fall outside the interval.  The
+ * events are cudaEvent_t values passed as void*; the hook is consumed by
+ * that one call.  Passing NULLs clears it.
+ */
+PA_API void pa_profile_next_call(void* start_event, void* stop_event);
+
+/* Library version and the number of kernels the last call enqueued. */
+PA_API int pa_version(void);
+PA_API int pa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H */

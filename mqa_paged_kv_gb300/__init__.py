@@ -1,0 +1,212 @@
+"""Python binding of libpaged_attn.so (paged-KV GQA/MQA attention, sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+The functions carry the C ABI's names (include/paged_attn.h) and take
+torch tensors for device memory and the current torch CUDA stream.  If the
+compiled library is missing this module raises at import; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpaged_attn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python mqa_paged_kv_gb300/build.py` "
+        "(nvcc, sm_103a); there is no CPU or library fallback")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PA_F16 = 0
+PA_BF16 = 1
+PA_DEV_BAD_BLOCK_ID = 0x1
+PA_DEV_BAD_SLOT = 0x2
+PA_DEV_WAIT_TIMEOUT = 0x4
+PA_DEV_BAD_LENGTHS = 0x8
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_lib.pa_status_string.argtypes = [_I]
+_lib.pa_status_string.restype = ctypes.c_char_p
+_lib.pa_version.argtypes = []
+_lib.pa_version.restype = _I
+_lib.pa_last_launch_count.argtypes = []
+_lib.pa_last_launch_count.restype = _I
+_lib.reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]
+_lib.reshape_and_cache.restype = _I
+_lib.paged_attn_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I, _I]
+_lib.paged_attn_workspace_bytes.restype = _SZ
+_lib.paged_attn_decode.argtypes = [_P, _P, _P, _P, _I, _P, _F, _I, _I, _I, _I, _I, _I, _I,
+                                   _I, _P, _P, _SZ, _P]
+_lib.paged_attn_decode.restype = _I
+_lib.paged_attn_chunked_prefill_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I]
+_lib.paged_attn_chunked_prefill_workspace_bytes.restype = _SZ
+_lib.paged_attn_chunked_prefill.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, _F, _I, _I,
+                                            _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+_lib.paged_attn_chunked_prefill.restype = _I
+_lib.pa_read_device_status.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]
+_lib.pa_read_device_status.restype = _I
+
+_lib.pa_profile_next_call.argtypes = [_P, _P]
+_lib.pa_profile_next_call.restype = None
+
+EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_launch_count", "reshape_and_cache",
+            "paged_attn_workspace_bytes", "paged_attn_decode",
+            "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
+            "pa_read_device_status"]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def status_string(status: int) -> str:
+    return _lib.pa_status_string(int(status)).decode()
+
+
+def last_launch_count() -> int:
+    return int(_lib.pa_last_launch_count())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    return -1
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise PagedAttnError(rc, where)
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                      status_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k, v [T, Hkv, D] -> k_cache, v_cache [NB, Hkv, bs, D] at slot_mapping
+    (int64, -1 skips)."""
+    _contig(k, v, k_cache, v_cache, slot_mapping)
+    T, Hkv, D = k.shape
+    NB, Hkv2, bs, D2 = k_cache.shape
+    if Hkv2 != Hkv or D2 != D or v.shape != k.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if slot_mapping.dtype != torch.int64 or k.dtype != k_cache.dtype:
+        raise ValueError("slot_mapping must be int64 and caches match k's dtype")
+    rc = _lib.reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(slot_mapping), T, Hkv, D, bs, NB, _dtype_code(k),
+                                _ptr(status_word), _stream(stream))
+    _check(rc, "reshape_and_cache")
+
+
+def paged_attn_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,
+                               head_dim: int, max_blocks_per_seq: int, block_size: int,
+                               num_splits: int = 0) -> int:
+    return int(_lib.paged_attn_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
+                                               max_blocks_per_seq, block_size, num_splits))
+
+
+def paged_attn_chunked_prefill_workspace_bytes(num_seqs: int, total_query_tokens: int,
+                                               num_heads: int, num_kv_heads: int,
+                                               head_dim: int, max_blocks_per_seq: int,
+                                               block_size: int, num_splits: int = 0) -> int:
+    return int(_lib.paged_attn_chunked_prefill_workspace_bytes(
+        num_seqs, total_query_tokens, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+        block_size, num_splits))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned workspace (torch's allocator aligns to 512 B)."""
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables [B, MBS] int32;
+    context_lens [B] int32 -> out [B, Hq, D]."""
+    _contig(q, k_cache, v_cache, block_tables, context_lens, out)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    mbs = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(
+            paged_attn_workspace_bytes(B, Hq, Hkv, D, mbs, bs, num_splits), q.device)
+    rc = _lib.paged_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mbs,
+                                _ptr(context_lens), float(scale), B, Hq, Hkv, D, bs, NB,
+                                _dtype_code(q), num_splits, _ptr(out), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "paged_attn_decode")
+    return out
+
+
+def paged_attn_chunked_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, cu_query_lens: torch.Tensor,
+                               context_lens: torch.Tensor, max_query_len: int, scale: float,
+                               out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """q [T, Hq, D] in the cu_query_lens layout -> out [T, Hq, D]."""
+    _contig(q, k_cache, v_cache, block_tables, cu_query_lens, context_lens, out)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    B = context_lens.shape[0]
+    mbs = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(paged_attn_chunked_prefill_workspace_bytes(
+            B, T, Hq, Hkv, D, mbs, bs, num_splits), q.device)
+    rc = _lib.paged_attn_chunked_prefill(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mbs, _ptr(cu_query_lens),
+        _ptr(context_lens), T, int(max_query_len), float(scale), B, Hq, Hkv, D, bs, NB,
+        _dtype_code(q), num_splits, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "paged_attn_chunked_prefill")
+    return out
+
+
+def pa_read_device_status(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    rc = _lib.pa_read_device_status(_ptr(workspace), int(bool(clear)), ctypes.byref(flags),
+                                    _stream(stream))
+    _check(rc, "pa_read_device_status")
+    return int(flags.value)
+
+
+def pa_profile_next_call(start_event, stop_event) -> None:
+    """Record two torch.cuda.Event objects around the attention kernels of
+    the next call on this thread (see include/paged_attn.h)."""
+    _lib.pa_profile_next_call(ctypes.c_void_p(start_event.cuda_event),
+                              ctypes.c_void_p(stop_event.cuda_event))

@@ -1,0 +1,532 @@
+// Paged GQA/MQA decode attention for sm_103a.
+//
+// Work unit: one (sequence, KV split, KV head) item.  The G query heads that
+// share the KV head are processed together, so each cache block of that KV
+// head is read from HBM once for all of them (vLLM issue #1880, "[Performance]
+// Use optimized kernels for MQA/GQA": the MQA/GQA saving only appears when
+// the kernel exploits the sharing; item 2 names the paged decode kernel).
+//
+// Structure:
+//  * persistent CTAs of 8 warps; warps form groups of ceil(G / 8) warps, and
+//    each group pulls items from a device work list with one atomic per item;
+//  * per group, a ring of R stages; a stage is a 16-key tile of K and V
+//    (one TMA box per 64 columns, 128-byte swizzle) plus, for the first tile
+//    of an item, the G query rows (one bulk copy); the first warp of the
+//    group issues the copies R stages ahead, so HBM reads of the next tiles
+//    (and of the next item) overlap the math on the current one;
+//  * the grouped dot products run on tensor cores with the KV tokens on the
+//    MMA's M side ("swap AB": S^T = K Q^T, O^T += V^T P^T) so a 16-key tile
+//    fills the 16 rows and the query heads sit on the 8-wide N side;
+//    P^T is turned into the B operand of the second MMA with movmatrix;
+//  * online softmax in base 2 with fp32 running max / sum per head column;
+//  * items that cover a whole sequence write the output row; split items
+//    write an fp32 partial and its log-sum-exp, merged by combine_kernel.
+#include "pa_kernels.cuh"
+
+namespace pa {
+
+namespace {
+
+struct StageMeta {
+  int32_t tok, kvh, key_base, nvalid, part_idx, flags, b, pad;
+};
+constexpr int kFirst = 1, kLast = 2, kDone = 4;
+
+template <int D, int GS>
+struct DecodeTile {
+  static constexpr int kBoxes = D / 64;       // 64-column TMA boxes per row
+  static constexpr int kKV = kBoxes * 2048;   // one 16-key tile of K (or V)
+  static constexpr int kQ = GS * 8 * D * 2;   // query rows of one group
+  static constexpr int kStage = 2 * kKV + kQ;
+  static_assert(kStage % 1024 == 0, "stages keep 1024-byte alignment");
+};
+
+template <int D, int GS, int NW, int R>
+struct DecodeSmem {
+  using T = DecodeTile<D, GS>;
+  static constexpr int kGroups = NW / GS;
+  static constexpr int kRing = kGroups * R * T::kStage;
+  static constexpr int kBars = kGroups * R * 2 * 8;
+  static constexpr int kMeta = kGroups * R * static_cast<int>(sizeof(StageMeta));
+  static constexpr int kBytes = kRing + kBars + kMeta + 1024;  // + alignment slack
+};
+
+// Producer-side description of the item whose tiles are being issued.
+struct Cursor {
+  int tok, b, kvh, key, key_end, part;
+  int ids, ids_base;  // lane l: physical block of logical block ids_base + l
+  bool first;
+};
+
+// The next item, fetched a step at a time while the current one is issued.
+struct Next {
+  int state;  // 0 none, 1 grabbed, 2 record loaded, 3 ready, 4 list exhausted
+  uint32_t it;
+  int kvh;
+  DecPair rec;
+  int ids;
+};
+
+}  // namespace
+
+template <bool kBF16, int D, int GS, int NW, int R>
+__global__ void __launch_bounds__(NW * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeParams p) {
+  using T = DecodeTile<D, GS>;
+  using S = DecodeSmem<D, GS, NW, R>;
+  constexpr int kMT = D / 16;  // 16-row MMA tiles along D
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int group = warp / GS, wig = warp % GS;
+  uint8_t* ring = smem + group * R * T::kStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kRing) + group * 2 * R;
+  uint64_t* empty = full + R;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + S::kRing + S::kBars) + group * R;
+
+  // Query slots start zeroed: rows past G are never written and feed the
+  // padded N columns of the MMA.
+  for (int i = threadIdx.x; i < S::kGroups * R * (T::kQ / 16); i += blockDim.x) {
+    const int st = i / (T::kQ / 16), c = i % (T::kQ / 16);
+    reinterpret_cast<uint4*>(smem + st * T::kStage + 2 * T::kKV)[c] = make_uint4(0, 0, 0, 0);
+  }
+  if (threadIdx.x == 0) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing);
+    for (int g = 0; g < S::kGroups; ++g)
+      for (int s = 0; s < R; ++s) {
+        mbar_init(bars + g * 2 * R + s, 1);
+        mbar_init(bars + g * 2 * R + R + s, GS);
+      }
+    fence_mbar_init();
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  fence_proxy_async();
+  __syncthreads();
+
+  const uint32_t num_items = p.hdr->decode_items;
+  const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
+  const bool producer = (wig == 0);
+  uint32_t* status = &p.hdr->status;
+  const uint16_t* qg = static_cast<const uint16_t*>(p.q);
+
+  // ---------------------------------------------------------------- producer
+  uint32_t p_iter = 0;
+  bool p_finished = false;
+  Cursor cur;
+  cur.key = cur.key_end = 0;
+  cur.ids = -1;
+  cur.ids_base = 0;
+  cur.first = false;
+  cur.tok = cur.b = cur.kvh = cur.part = 0;
+  Next nx;
+  nx.state = 0;
+  nx.it = 0;
+  nx.kvh = 0;
+  nx.ids = -1;
+
+  auto load_ids = [&](int b, int lblk0, int key_end) -> int {
+    const int lb = lblk0 + lane;
+    if (lb * bs < key_end) return __ldg(p.block_tables + static_cast<int64_t>(b) * p.mbs + lb);
+    return -1;
+  };
+
+  auto advance = [&]() {
+    if (nx.state == 0) {
+      uint32_t it = 0;
+      if (lane == 0) it = atomicAdd(&p.hdr->decode_grab, 1u);
+      nx.it = it;
+      nx.state = 1;
+    } else if (nx.state == 1) {
+      const uint32_t it = __shfl_sync(0xffffffffu, nx.it, 0);
+      if (it >= num_items) {
+        nx.state = 4;
+      } else {
+        const uint32_t pair = it / static_cast<uint32_t>(Hkv);
+        nx.kvh = static_cast<int>(it - pair * static_cast<uint32_t>(Hkv));
+        const int4* rp = reinterpret_cast<const int4*>(p.pairs + pair);
+        const int4 r0 = __ldg(rp), r1 = __ldg(rp + 1);
+        nx.rec.b = r0.x;
+        nx.rec.tok = r0.y;
+        nx.rec.key_begin = r0.z;
+        nx.rec.key_end = r0.w;
+        nx.rec.part_idx = r1.x;
+        nx.state = 2;
+      }
+    } else if (nx.state == 2) {
+      nx.ids = load_ids(nx.rec.b, nx.rec.key_begin / bs, nx.rec.key_end);
+      nx.state = 3;
+    }
+  };
+
+  auto issue_stage = [&]() {
+    if (p_finished) return;
+    const int s = static_cast<int>(p_iter % R);
+    if (GS > 1 && p_iter >= static_cast<uint32_t>(R)) {
+      if (!mbar_wait(&empty[s], ((p_iter / R) - 1) & 1)) {
+        if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
+        p_finished = true;
+        return;
+      }
+    }
+    if (cur.key >= cur.key_end) {
+      while (nx.state < 3) advance();
+      if (nx.state == 4) {
+        if (lane == 0) {
+          meta[s].flags = kDone;
+          mbar_arrive(&full[s]);
+        }
+        p_finished = true;
+        ++p_iter;
+        return;
+      }
+      cur.tok = nx.rec.tok;
+      cur.b = nx.rec.b;
+      cur.kvh = nx.kvh;
+      cur.key = nx.rec.key_begin;
+      cur.key_end = nx.rec.key_end;
+      cur.part = nx.rec.part_idx;
+      cur.ids = nx.ids;
+      cur.ids_base = nx.rec.key_begin / bs;
+      cur.first = true;
+      nx.state = 0;
+    }
+    const int key_base = cur.key;
+    int nvalid = cur.key_end - key_base;
+    if (nvalid > kKeyTile) nvalid = kKeyTile;
+    const int lblk = key_base / bs;
+    if (lblk - cur.ids_base >= 32) {
+      cur.ids_base = lblk;
+      cur.ids = load_ids(cur.b, lblk, cur.key_end);
+    }
+    int blk = __shfl_sync(0xffffffffu, cur.ids, lblk - cur.ids_base);
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (lane == 0) Status::raise(status, PA_DEV_BAD_BLOCK_ID);
+      blk = 0;
+      nvalid = 0;
+    }
+    const int y = (blk * Hkv + cur.kvh) * bs + (key_base - lblk * bs);
+    const bool first = cur.first;
+    const bool last = key_base + kKeyTile >= cur.key_end;
+    if (lane == 0) {
+      StageMeta m;
+      m.tok = cur.tok;
+      m.kvh = cur.kvh;
+      m.key_base = key_base;
+      m.nvalid = nvalid;
+      m.part_idx = cur.part;
+      m.flags = (first ? kFirst : 0) | (last ? kLast : 0);
+      m.b = cur.b;
+      m.pad = 0;
+      meta[s] = m;
+      const uint32_t qbytes = first ? static_cast<uint32_t>(G * D * 2) : 0u;
+      mbar_arrive_expect_tx(&full[s], 2 * T::kKV + qbytes);
+      uint8_t* st = ring + s * T::kStage;
+#pragma unroll
+      for (int bx = 0; bx < T::kBoxes; ++bx) {
+        tma_load_2d(st + bx * 2048, &tmk, bx * 64, y, &full[s]);
+        tma_load_2d(st + T::kKV + bx * 2048, &tmv, bx * 64, y, &full[s]);
+      }
+      if (first) {
+        const uint16_t* src =
+            qg + (static_cast<int64_t>(cur.tok) * Hq + static_cast<int64_t>(cur.kvh) * G) * D;
+        bulk_load(st + 2 * T::kKV, src, qbytes, &full[s]);
+      }
+    }
+    cur.key += kKeyTile;
+    cur.first = false;
+    ++p_iter;
+    if (nx.state < 3) advance();
+  };
+
+  // ---------------------------------------------------------------- consumer
+  const int g = lane >> 2, q4 = lane & 3;
+  const int mi = lane >> 3, rr = lane & 7;
+  float acc[kMT][4];
+  float mrow[2], lrow[2];
+  uint32_t qf[kMT][2];
+#pragma unroll
+  for (int i = 0; i < kMT; ++i) {
+    acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    qf[i][0] = qf[i][1] = 0u;
+  }
+  mrow[0] = mrow[1] = -INFINITY;
+  lrow[0] = lrow[1] = 0.f;
+
+  auto finalize = [&](const StageMeta& m) {
+    float l0 = lrow[0], l1 = lrow[1];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const float il0 = l0 > 0.f ? 1.f / l0 : 0.f;
+    const float il1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    const int hb = 8 * wig;
+    if (m.part_idx < 0) {
+      uint16_t* out = static_cast<uint16_t*>(p.out) +
+                      (static_cast<int64_t>(m.tok) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+      const int h = hb + g;
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const uint32_t t0 =
+            movmatrix_t(pack2<kBF16>(acc[mt][0] * il0, acc[mt][1] * il1));
+        const uint32_t t1 =
+            movmatrix_t(pack2<kBF16>(acc[mt][2] * il0, acc[mt][3] * il1));
+        if (h < G) {
+          uint32_t* o = reinterpret_cast<uint32_t*>(out + h * D + mt * 16 + 2 * q4);
+          o[0] = t0;
+          o[4] = t1;  // +8 elements
+        }
+      }
+    } else {
+      float* po = p.part_o +
+                  (static_cast<int64_t>(m.part_idx) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+      const int h0 = hb + 2 * q4, h1 = h0 + 1;
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int d0 = mt * 16 + g, d1 = d0 + 8;
+        if (h0 < G) {
+          po[h0 * D + d0] = acc[mt][0] * il0;
+          po[h0 * D + d1] = acc[mt][2] * il0;
+        }
+        if (h1 < G) {
+          po[h1 * D + d0] = acc[mt][1] * il1;
+          po[h1 * D + d1] = acc[mt][3] * il1;
+        }
+      }
+      if (g == 0) {
+        float* pl = p.part_lse + static_cast<int64_t>(m.part_idx) * Hq +
+                    static_cast<int64_t>(m.kvh) * G;
+        if (h0 < G) pl[h0] = l0 > 0.f ? mrow[0] + __log2f(l0) : -INFINITY;
+        if (h1 < G) pl[h1] = l1 > 0.f ? mrow[1] + __log2f(l1) : -INFINITY;
+      }
+    }
+  };
+
+  if (producer)
+    for (int i = 0; i < R; ++i) issue_stage();
+
+  uint32_t c_iter = 0;
+  while (true) {
+    const int s = static_cast<int>(c_iter % R);
+    if (!mbar_wait(&full[s], (c_iter / R) & 1)) {
+      if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
+      break;
+    }
+    const StageMeta m = meta[s];
+    if (m.flags & kDone) break;
+    const uint32_t kbase = smem_u32(ring + s * T::kStage);
+    const uint32_t vbase = kbase + T::kKV;
+    const uint32_t qbase = kbase + 2 * T::kKV;
+
+    if (m.flags & kFirst) {
+#pragma unroll
+      for (int i = 0; i < kMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      mrow[0] = mrow[1] = -INFINITY;
+      lrow[0] = lrow[1] = 0.f;
+      // B operand (Q^T): rows = this warp's 8 heads, 16-byte chunks along D.
+#pragma unroll
+      for (int ks = 0; ks < kMT; ks += 2) {
+        const int row = 8 * wig + rr;
+        const int chunk = 2 * ks + mi;
+        uint32_t r[4];
+        ldsm_x4(qbase + row * (D * 2) + chunk * 16, r);
+        qf[ks][0] = r[0];
+        qf[ks][1] = r[1];
+        qf[ks + 1][0] = r[2];
+        qf[ks + 1][1] = r[3];
+      }
+    }
+
+    // S^T[16 keys][8 heads] = K Q^T, two accumulation chains.
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < kMT; ++ks) {
+      const int key = rr + ((mi & 1) << 3);
+      const int chunk = ((ks & 3) << 1) + (mi >> 1);
+      uint32_t a[4];
+      ldsm_x4(kbase + (ks >> 2) * 2048 + swz128(key, chunk), a);
+      if (ks & 1)
+        mma_16816<kBF16>(sb, a, qf[ks][0], qf[ks][1]);
+      else
+        mma_16816<kBF16>(sa, a, qf[ks][0], qf[ks][1]);
+    }
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = (sa[i] + sb[i]) * p.scale_log2;
+    const int nv = m.nvalid;
+    if (nv < kKeyTile) {
+      if (g >= nv) x[0] = x[1] = -INFINITY;
+      if (g + 8 >= nv) x[2] = x[3] = -INFINITY;
+    }
+
+    // Online softmax per head column (this lane: heads 2*q4, 2*q4 + 1).
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(mrow[0], mx0), mn1 = fmaxf(mrow[1], mx1);
+    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = ex2(mrow[0] - ref0), al1 = ex2(mrow[1] - ref1);
+    mrow[0] = mn0;
+    mrow[1] = mn1;
+    const uint32_t ptop = pack2<kBF16>(ex2(x[0] - ref0), ex2(x[1] - ref1));
+    const uint32_t pbot = pack2<kBF16>(ex2(x[2] - ref0), ex2(x[3] - ref1));
+    float p00, p01, p10, p11;
+    unpack2<kBF16>(ptop, p00, p01);
+    unpack2<kBF16>(pbot, p10, p11);
+    lrow[0] = lrow[0] * al0 + (p00 + p10);
+    lrow[1] = lrow[1] * al1 + (p01 + p11);
+    const uint32_t b0 = movmatrix_t(ptop);  // P^T rows: keys 2*q4.., column: head g
+    const uint32_t b1 = movmatrix_t(pbot);  // keys 8 + 2*q4..
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+
+    // O^T[D][8 heads] += V^T P^T.
+    const uint32_t vm_lo = keep_mask(2 * q4 < nv, 2 * q4 + 1 < nv);
+    const uint32_t vm_hi = keep_mask(8 + 2 * q4 < nv, 9 + 2 * q4 < nv);
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) {
+      const int key = rr + ((mi >> 1) << 3);
+      const int chunk = ((mt & 3) << 1) + (mi & 1);
+      uint32_t a[4];
+      ldsm_x4_t(vbase + (mt >> 2) * 2048 + swz128(key, chunk), a);
+      if (nv < kKeyTile) {
+        a[0] &= vm_lo;
+        a[1] &= vm_lo;
+        a[2] &= vm_hi;
+        a[3] &= vm_hi;
+      }
+      mma_16816<kBF16>(acc[mt], a, b0, b1);
+    }
+
+    __syncwarp();
+    if (GS > 1 && lane == 0) mbar_arrive(&empty[s]);
+    if (producer) issue_stage();
+    if (m.flags & kLast) finalize(m);
+    ++c_iter;
+  }
+
+  // Leave no copy in flight: wait (bounded) for stages this group issued but
+  // did not consume, so the CTA never exits with TMA writes pending.
+  if (producer) {
+    while (c_iter < p_iter) {
+      const int s = static_cast<int>(c_iter % R);
+      if (!mbar_wait(&full[s], (c_iter / R) & 1)) break;
+      ++c_iter;
+    }
+  }
+}
+
+// Merge the split partials of each decode sequence:
+//   M = max_s lse_s, w_s = 2^(lse_s - M), out = sum_s w_s o_s / sum_s w_s,
+// with lse kept in base 2 and splits of lse = -inf weighted 0.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
+  const int b = blockIdx.x;
+  const SeqInfo si = p.seq_info[b];
+  if (si.qlen != 1 || si.nsplit <= 1) return;
+  const int Hq = p.num_heads, D = p.head_dim, S = si.nsplit;
+  const float* lse = p.part_lse + static_cast<int64_t>(si.split_offset) * Hq;
+  const float* po = p.part_o + static_cast<int64_t>(si.split_offset) * Hq * D;
+  uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(si.tok) * Hq * D;
+  const int per_head = D / 4;
+  for (int i = threadIdx.x; i < Hq * per_head; i += blockDim.x) {
+    const int h = i / per_head, d4 = i - h * per_head;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, lse[s * Hq + h]);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, wsum = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < S; ++s) {
+        const float ls = lse[s * Hq + h];
+        if (ls == -INFINITY) continue;
+        const float w = ex2(ls - M);
+        const float4 v =
+            reinterpret_cast<const float4*>(po + (static_cast<int64_t>(s) * Hq + h) * D)[d4];
+        wsum += w;
+        a0 += w * v.x;
+        a1 += w * v.y;
+        a2 += w * v.z;
+        a3 += w * v.w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint2 o;
+    o.x = pack2<kBF16>(a0 * inv, a1 * inv);
+    o.y = pack2<kBF16>(a2 * inv, a3 * inv);
+    reinterpret_cast<uint2*>(out + h * D)[d4] = o;
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+namespace {
+
+template <bool kBF16, int D, int GS>
+int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                    cudaStream_t stream, int num_sms) {
+  constexpr int NW = 8;
+  constexpr int kStageBytes = DecodeTile<D, GS>::kStage;
+  constexpr int kBudget = 160 * 1024;
+  constexpr int kGroups = NW / GS;
+  constexpr int kR0 = kBudget / (kGroups * kStageBytes);
+  constexpr int R = kR0 < 2 ? 2 : (kR0 > 8 ? 8 : kR0);
+  using S = DecodeSmem<D, GS, NW, R>;
+  static_assert(S::kBytes <= 227 * 1024, "fits one CTA per SM");
+  auto kern = decode_kernel<kBF16, D, GS, NW, R>;
+  static int configured = -1;  // device whose attribute is set
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) !=
+        cudaSuccess)
+      return -1;
+    configured = dev;
+  }
+  kern<<<num_sms, NW * 32, S::kBytes, stream>>>(tmk, tmv, p);
+  return 1;
+}
+
+template <bool kBF16, int D>
+int launch_decode_d(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                    cudaStream_t stream, int num_sms) {
+  const int gs = (p.G + 7) / 8;
+  if (gs <= 1) return launch_decode_t<kBF16, D, 1>(tmk, tmv, p, stream, num_sms);
+  if (gs <= 2) return launch_decode_t<kBF16, D, 2>(tmk, tmv, p, stream, num_sms);
+  if (gs <= 4) return launch_decode_t<kBF16, D, 4>(tmk, tmv, p, stream, num_sms);
+  return launch_decode_t<kBF16, D, 8>(tmk, tmv, p, stream, num_sms);
+}
+
+}  // namespace
+
+int launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                  bool bf16, int head_dim, cudaStream_t stream, int num_sms) {
+  if (bf16) {
+    return head_dim == 64 ? launch_decode_d<true, 64>(tmk, tmv, p, stream, num_sms)
+                          : launch_decode_d<true, 128>(tmk, tmv, p, stream, num_sms);
+  }
+  return head_dim == 64 ? launch_decode_d<false, 64>(tmk, tmv, p, stream, num_sms)
+                        : launch_decode_d<false, 128>(tmk, tmv, p, stream, num_sms);
+}
+
+int launch_combine(const CombineParams& p, bool bf16, cudaStream_t stream) {
+  if (p.num_seqs <= 0) return 0;
+  if (bf16)
+    combine_kernel<true><<<p.num_seqs, 256, 0, stream>>>(p);
+  else
+    combine_kernel<false><<<p.num_seqs, 256, 0, stream>>>(p);
+  return 1;
+}
+
+}  // namespace pa

@@ -1,0 +1,167 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels:
+// workspace layout, work-item records and launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+// ------------------------------------------------------------------ sizes
+constexpr int kKeyTile = 16;          // keys per decode pipeline stage
+constexpr int kAutoSplitTokens = 256; // automatic split length (tokens)
+constexpr int kMaxSplits = 64;        // splits per sequence, at most
+constexpr int kPrefillRows = 64;      // (token, head) rows per prefill tile
+constexpr int kPrefillKeys = 64;      // keys per prefill pipeline stage
+
+// ------------------------------------------------------------------ records
+// Header at the start of every workspace (256 bytes).
+struct WsHeader {
+  uint32_t decode_grab;      // next decode item to hand out
+  uint32_t status;           // PA_DEV_* bits of the most recent call
+  uint32_t decode_items;     // decode (split, kv head) items
+  uint32_t decode_pairs;     // decode (sequence, split) pairs
+  uint32_t prefill_grab;     // next prefill item to hand out
+  uint32_t prefill_items;    // prefill (tile, kv head) items
+  uint32_t prefill_tiles;
+  uint32_t pad[57];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Per sequence: where its split partials live and how its query rows map.
+struct SeqInfo {
+  int32_t split_offset;  // first partial index of this sequence's splits
+  int32_t nsplit;        // decode splits (0: no decode row; 1: no combine)
+  int32_t tok;           // query row of a decode sequence
+  int32_t qlen;
+};
+
+// A decode (sequence, split) pair; item = pair * Hkv + kv head.
+struct DecPair {
+  int32_t b;
+  int32_t tok;        // query / output row
+  int32_t key_begin;  // first key (multiple of the block size)
+  int32_t key_end;    // one past the last key
+  int32_t part_idx;   // partial slot, or -1 when the split is the whole sequence
+  int32_t pad[3];
+};
+
+// A prefill tile: up to kPrefillRows / G query tokens of one sequence;
+// item = tile * Hkv + kv head.
+struct PfTile {
+  int32_t b;
+  int32_t tok0;   // first query row of the tile
+  int32_t ntok;   // valid query tokens in the tile
+  int32_t pos0;   // absolute position of the first token (ctx - qlen + i)
+};
+
+struct WsLayout {
+  size_t seq_info, pairs, part_lse, part_o, tiles, total;
+  int64_t max_pairs, max_tiles;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Upper bound of KV splits of one sequence (host side, no device data).
+inline int64_t max_splits_per_seq(int max_blocks_per_seq, int block_size, int num_splits) {
+  if (num_splits > 0) return num_splits;
+  const int64_t chunk = (kAutoSplitTokens + block_size - 1) / block_size;
+  int64_t s = (max_blocks_per_seq + chunk - 1) / chunk;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  return s;
+}
+
+inline int prefill_tokens_per_tile(int G) {
+  const int t = kPrefillRows / G;
+  return t < 1 ? 1 : t;
+}
+
+inline WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int64_t max_pairs,
+                                 int64_t max_tiles) {
+  WsLayout L;
+  size_t off = sizeof(WsHeader);
+  L.seq_info = off;
+  off = align_up(off + sizeof(SeqInfo) * static_cast<size_t>(num_seqs), 256);
+  L.pairs = off;
+  off = align_up(off + sizeof(DecPair) * static_cast<size_t>(max_pairs), 256);
+  L.part_lse = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(max_pairs) * num_heads, 256);
+  L.part_o = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(max_pairs) * num_heads * head_dim, 256);
+  L.tiles = off;
+  off = align_up(off + sizeof(PfTile) * static_cast<size_t>(max_tiles), 256);
+  L.total = off;
+  L.max_pairs = max_pairs;
+  L.max_tiles = max_tiles;
+  return L;
+}
+
+// ------------------------------------------------------------------ params
+struct PrepareParams {
+  const int32_t* context_lens;
+  const int32_t* cu_query_lens;  // nullptr: pure decode (qlen 1, row = b)
+  void* out;                     // zero rows of empty decode sequences
+  WsHeader* hdr;
+  SeqInfo* seq_info;
+  DecPair* pairs;
+  PfTile* tiles;
+  int num_seqs, block_size, num_splits, num_kv_heads, num_heads, head_dim;
+  int tokens_per_tile;  // prefill tile height in tokens
+  int max_blocks_per_seq;
+  int64_t total_tokens;  // rows of q / out
+};
+
+struct DecodeParams {
+  const void* q;
+  const int32_t* block_tables;
+  void* out;
+  float* part_o;
+  float* part_lse;
+  const DecPair* pairs;
+  WsHeader* hdr;
+  int mbs, num_heads, num_kv_heads, G, block_size, num_blocks;
+  float scale_log2;  // scale * log2(e)
+};
+
+struct CombineParams {
+  const SeqInfo* seq_info;
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  int num_seqs, num_heads, head_dim;
+};
+
+struct PrefillParams {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  const PfTile* tiles;
+  WsHeader* hdr;
+  int mbs, num_heads, num_kv_heads, G, block_size, num_blocks, tokens_per_tile;
+  float scale_log2;
+};
+
+// ------------------------------------------------------------------ launchers
+// Each returns the number of kernels enqueued, or -1 on a launch error.
+int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks, uint32_t* status,
+                             cudaStream_t stream, int num_sms);
+
+int launch_prepare(const PrepareParams& p, bool bf16, cudaStream_t stream);
+
+int launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
+                  bool bf16, int head_dim, cudaStream_t stream, int num_sms);
+
+int launch_combine(const CombineParams& p, bool bf16, cudaStream_t stream);
+
+int launch_prefill(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                   const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
+                   cudaStream_t stream, int num_sms);
+
+}  // namespace pa

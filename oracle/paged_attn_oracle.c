@@ -322,7 +322,9 @@ static int orc_check(const orc_problem* P)
     for (int b = 0; b < P->B; ++b) {
         int ql = P->cu_query_lens[b + 1] - P->cu_query_lens[b];
         int ctx = P->context_lens[b];
-        if (ql < 0 || ctx < ql || ctx > P->mbs * P->bs)
+        /* a sequence with no cached key may still carry query rows: they
+         * read nothing and are zero */
+        if (ql < 0 || ctx < 0 || (ctx < ql && ctx != 0) || ctx > P->mbs * P->bs)
             return ORC_ERR_ARG;
     }
     return ORC_OK;
@@ -399,6 +401,24 @@ int orc_paged_attention(const uint16_t* q, const uint16_t* k_cache,
             int t = (int)(tok - cu_query_lens[b]);
             int p = ctx - qlen + t; /* absolute position of this query token */
             int n = p + 1;          /* keys 0..p are visible */
+            if (ctx == 0) {         /* no key at all: zero row, empty splits */
+                int64_t zb = (r * Hq + h) * (int64_t)D;
+                for (int d = 0; d < D; ++d) {
+                    out64[zb + d] = 0.0;
+                    if (out_bits)
+                        out_bits[zb + d] = 0;
+                }
+                if (S > 1 && (part_o || part_lse))
+                    for (int sp = 0; sp < S; ++sp) {
+                        int64_t pi = (r * Hq + h) * (int64_t)S + sp;
+                        if (part_lse)
+                            part_lse[pi] = -INFINITY;
+                        if (part_o)
+                            for (int d = 0; d < D; ++d)
+                                part_o[pi * D + d] = 0.0;
+                    }
+                continue;
+            }
             if (n > cap) {
                 free(Kh); free(Vh); free(s);
                 cap = n;

@@ -1,0 +1,116 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+that include/paged_attn.h declares, sizes workspaces, and rejects invalid
+arguments on the host with the documented status codes before touching any
+device state."""
+import ctypes
+import re
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__._load_build_module().build()
+    import mqa_paged_kv_gb300 as pa
+    return pa
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "paged_attn.h")) as f:
+        text = f.read()
+    return re.findall(r"PA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = set(_declared_functions())
+    assert {"paged_attn_decode", "paged_attn_chunked_prefill", "reshape_and_cache",
+            "paged_attn_workspace_bytes", "pa_status_string"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(so, name), name
+    assert set(_declared_functions()) == set(lib.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(-9, 1):
+        assert lib.status_string(code) != "unknown status"
+    assert lib.status_string(-99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    a = lib.paged_attn_workspace_bytes(256, 32, 8, 128, 256, 16, 0)
+    b = lib.paged_attn_workspace_bytes(256, 32, 8, 128, 256, 16, 1)
+    c = lib.paged_attn_workspace_bytes(8, 32, 8, 128, 2048, 16, 0)
+    assert a > b > 0 and c > 0
+    # auto splits cap at 64 per sequence: 8 seqs x 64 splits x 32 heads x (128 + 1) floats
+    assert c >= 8 * 64 * 32 * 129 * 4
+    assert lib.paged_attn_chunked_prefill_workspace_bytes(64, 4434, 32, 8, 128, 256, 16, 0) > 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails host validation
+
+
+def _decode(lib, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mbs=4, ctx=FAKE, scale=0.125, B=2, Hq=8,
+                Hkv=2, D=64, bs=16, NB=8, dtype=1, S=0, out=FAKE, ws=FAKE, wsb=1 << 30)
+    args.update(kw)
+    a = args
+    return lib._lib.paged_attn_decode(a["q"], a["k"], a["v"], a["bt"], a["mbs"], a["ctx"],
+                                      a["scale"], a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"],
+                                      a["NB"], a["dtype"], a["S"], a["out"], a["ws"], a["wsb"],
+                                      None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), -3), (dict(D=96), -4), (dict(D=256), -4), (dict(bs=8), -5),
+    (dict(bs=24), -5), (dict(bs=512), -5), (dict(Hq=6, Hkv=4), -2), (dict(Hkv=0), -2),
+    (dict(Hq=130, Hkv=2), -2), (dict(S=65), -2), (dict(S=-1), -2), (dict(B=-1), -2),
+    (dict(scale=float("nan")), -2), (dict(mbs=0), -2), (dict(NB=0), -2),
+    (dict(q=None), -1), (dict(out=None), -1), (dict(bt=None), -1),
+    (dict(q=FAKE + 8), -8), (dict(k=FAKE + 2), -8),
+    (dict(ws=None), -6), (dict(ws=FAKE + 16), -6), (dict(wsb=16), -6),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert _decode(lib, **kw) == code
+    assert lib.last_launch_count() == 0
+
+
+def test_decode_with_no_sequences_is_a_no_op(lib):
+    assert _decode(lib, B=0, q=None, out=None) == 0
+    assert lib.last_launch_count() == 0
+
+
+def test_chunked_prefill_rejects_bad_arguments(lib):
+    f = lib._lib.paged_attn_chunked_prefill
+    base = [FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 10, 5, 0.125, 2, 8, 2, 128, 16, 8, 1, 0,
+            FAKE, FAKE, 1 << 30, None]
+    a = list(base); a[5] = None                     # cu_query_lens
+    assert f(*a) == -1
+    a = list(base); a[7] = -1                       # total_query_tokens
+    assert f(*a) == -2
+    a = list(base); a[13] = 80                      # head_dim
+    assert f(*a) == -4
+    a = list(base); a[20] = 64                      # workspace too small
+    assert f(*a) == -6
+
+
+def test_reshape_and_cache_rejects_bad_arguments(lib):
+    f = lib._lib.reshape_and_cache
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 8, 1, None, None]
+    a = list(base); a[10] = 7
+    assert f(*a) == -3
+    a = list(base); a[7] = 32
+    assert f(*a) == -4
+    a = list(base); a[4] = None
+    assert f(*a) == -1
+    a = list(base); a[0] = FAKE + 4
+    assert f(*a) == -8
+    a = list(base); a[5] = 0
+    assert f(*a) == 0

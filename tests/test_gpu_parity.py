@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every test runs the whole step -- reshape_and_cache of the step's new tokens,
+then paged attention -- on seeded synthetic inputs.  reshape_and_cache must
+match the oracle bit for bit over the whole cache; attention must stay
+within max-abs 1e-2 (vs fp64) and mean-abs 1e-3 (vs the oracle rounded to
+the element type).  Small cases compare every output row; the full-size
+workloads compare sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_harness import GpuCase, bits, check_attention, run_and_check
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows_sample(case, n, seed=0):
+    rng = np.random.default_rng(seed)
+    T = case.total_query_tokens
+    return np.sort(rng.choice(T, size=min(n, T), replace=False))
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_gqa_decode(seed):
+    run_and_check(W.tiny_gqa_decode(seed))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_llama8b_decode_small(seed):
+    run_and_check(W.llama8b_decode(seed, batch=24, max_ctx=1024))
+
+
+def test_llama8b_decode_full_size_sampled():
+    c = W.llama8b_decode(0)
+    run_and_check(c, rows=_rows_sample(c, 48))
+
+
+@pytest.mark.parametrize("hkv", [1, 8, 32])
+def test_head_sweep_small(hkv):
+    run_and_check(W.head_sweep(0, num_kv_heads=hkv, batch=6))
+
+
+@pytest.mark.parametrize("hkv", [1, 8, 32])
+def test_head_sweep_full_size_sampled(hkv):
+    c = W.head_sweep(1, num_kv_heads=hkv)
+    run_and_check(c, rows=_rows_sample(c, 12))
+
+
+@pytest.mark.parametrize("splits", [0, 16, 32, 64])
+def test_long_context_split_kv(splits):
+    run_and_check(W.long_context_decode(0, batch=2), num_splits=splits)
+
+
+def test_long_context_full_size():
+    run_and_check(W.long_context_decode(1))
+
+
+# ---------------------------------------------------------------- mixed
+def _small_mixed(seed, **kw):
+    args = dict(n_prefill=3, n_decode=5, q_range=(2, 150), prior_range=(0, 300),
+                dec_range=(1, 700))
+    args.update(kw)
+    return W.mixed_prefill_decode(seed, **args)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_mixed_small(seed):
+    run_and_check(_small_mixed(seed))
+
+
+def test_mixed_full_size_sampled():
+    c = W.mixed_prefill_decode(0)
+    ql = c.query_lens
+    dec_rows = c.cu_query_lens[:-1][ql == 1]
+    last_rows = c.cu_query_lens[1:][ql > 1] - 1   # last token of each chunk
+    first_rows = c.cu_query_lens[:-1][ql > 1]
+    rows = np.unique(np.concatenate([dec_rows, last_rows, first_rows,
+                                     _rows_sample(c, 96, seed=3)]))
+    run_and_check(c, rows=rows)
+
+
+# ---------------------------------------------------------------- shapes
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 16, 32, 64])
+def test_group_sizes_decode_and_prefill(G):
+    rng = np.random.default_rng(G)
+    hkv = 2 if G <= 16 else 1
+    B = 5
+    ctx = rng.integers(1, 400, size=B)
+    ql = np.minimum(ctx, np.array([1, 1, 37, 1, 9]))
+    c = W.make_case(f"g{G}", seed=G, dtype=W.BF16, num_heads=G * hkv, num_kv_heads=hkv,
+                    head_dim=128, block_size=16, context_lens=ctx, query_lens=ql)
+    run_and_check(c)
+    d = W.make_case(f"g{G}d", seed=G + 100, dtype=W.BF16, num_heads=G * hkv,
+                    num_kv_heads=hkv, head_dim=128, block_size=16, context_lens=ctx,
+                    query_lens=np.ones(B, np.int64))
+    run_and_check(d)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128, 256])
+def test_block_sizes(bs):
+    rng = np.random.default_rng(bs)
+    ctx = rng.integers(1, 1200, size=6)
+    ql = np.minimum(ctx, np.array([1, 70, 1, 3, 1, 130]))
+    c = W.make_case(f"bs{bs}", seed=bs, dtype=W.BF16, num_heads=16, num_kv_heads=4,
+                    head_dim=128, block_size=bs, context_lens=ctx, query_lens=ql)
+    run_and_check(c)
+    d = W.make_case(f"bs{bs}d", seed=bs + 1, dtype=W.BF16, num_heads=16, num_kv_heads=4,
+                    head_dim=128, block_size=bs, context_lens=ctx,
+                    query_lens=np.ones(6, np.int64))
+    run_and_check(d, num_splits=3)
+
+
+@pytest.mark.parametrize("dtype,D", [(W.F16, 64), (W.F16, 128), (W.BF16, 64)])
+def test_dtypes_and_head_dims(dtype, D):
+    rng = np.random.default_rng(D + dtype)
+    ctx = rng.integers(1, 900, size=7)
+    ql = np.minimum(ctx, np.array([1, 1, 64, 1, 17, 1, 2]))
+    c = W.make_case("dt", seed=3, dtype=dtype, num_heads=8, num_kv_heads=2, head_dim=D,
+                    block_size=16, context_lens=ctx, query_lens=ql)
+    run_and_check(c)
+    d = W.make_case("dtd", seed=4, dtype=dtype, num_heads=8, num_kv_heads=2, head_dim=D,
+                    block_size=16, context_lens=ctx, query_lens=np.ones(7, np.int64))
+    run_and_check(d)
+
+
+# ---------------------------------------------------------------- edges
+def test_empty_and_one_token_contexts():
+    ctx = np.array([0, 1, 16, 17, 0, 33])
+    ql = np.array([0, 1, 1, 1, 0, 1])
+    c = W.make_case("edge", seed=5, dtype=W.BF16, num_heads=8, num_kv_heads=2, head_dim=128,
+                    block_size=16, context_lens=ctx, query_lens=ql, is_decode=False)
+    run_and_check(c)
+    # decode entry point: an empty sequence gets a zero row
+    d = W.make_case("edged", seed=6, dtype=W.BF16, num_heads=8, num_kv_heads=2,
+                    head_dim=128, block_size=16, context_lens=np.array([3, 1, 40]),
+                    query_lens=np.ones(3, np.int64))
+    d.context_lens[0] = 0
+    d.slot_mapping[0] = -1           # nothing to write for it
+    g = GpuCase(d)
+    g.write_cache()
+    out = g.attention()
+    torch.cuda.synchronize()
+    assert not bits(out)[0].any()
+    o64, ob, _, _ = oracle.run_case(d, rows=np.array([1, 2]))
+    check_attention(bits(out)[1:], o64, ob, d.dtype)
+
+
+def test_whole_chunk_in_one_sequence_and_qlen_equal_ctx():
+    ctx = np.array([300, 77])
+    ql = np.array([300, 77])          # no cached prefix: pure causal prefill
+    c = W.make_case("pure", seed=7, dtype=W.BF16, num_heads=32, num_kv_heads=8,
+                    head_dim=128, block_size=16, context_lens=ctx, query_lens=ql)
+    run_and_check(c)
+
+
+# ---------------------------------------------------------------- invariants
+def test_block_permutation_is_bitwise_invariant():
+    c = W.llama8b_decode(4, batch=16, max_ctx=900)
+    g1 = GpuCase(c)
+    g1.write_cache()
+    o1 = bits(g1.attention())
+    rng = np.random.default_rng(11)
+    perm = rng.permutation(c.num_blocks)
+    c2 = W.make_case("p", seed=0, dtype=c.dtype, num_heads=c.num_heads,
+                     num_kv_heads=c.num_kv_heads, head_dim=c.head_dim,
+                     block_size=c.block_size, context_lens=c.context_lens,
+                     query_lens=c.query_lens)
+    c2.q = c.q
+    c2.k_cache = np.empty_like(c.k_cache)
+    c2.v_cache = np.empty_like(c.v_cache)
+    c2.k_cache[perm] = c.k_cache
+    c2.v_cache[perm] = c.v_cache
+    c2.block_tables = np.where(c.block_tables >= 0, perm[np.maximum(c.block_tables, 0)], -1
+                               ).astype(np.int32)
+    bs = c.block_size
+    c2.slot_mapping = perm[c.slot_mapping // bs] * bs + c.slot_mapping % bs
+    c2.k_new, c2.v_new = c.k_new, c.v_new
+    g2 = GpuCase(c2)
+    g2.write_cache()
+    o2 = bits(g2.attention())
+    assert np.array_equal(o1, o2)
+
+
+def test_split_count_independence():
+    c = W.llama8b_decode(5, batch=12, max_ctx=3000)
+    g = GpuCase(c)
+    g.write_cache()
+    o64, ob, _, _ = oracle.run_case(c)
+    outs = {}
+    for s in [1, 2, 5, 17, 64, 0]:
+        outs[s] = bits(g.attention(num_splits=s))
+        check_attention(outs[s], o64, ob, c.dtype)
+    assert np.array_equal(outs[1], bits(g.attention(num_splits=1)))   # deterministic
+
+
+def test_chunked_entry_with_only_decode_rows_equals_decode_bitwise():
+    c = W.llama8b_decode(6, batch=20, max_ctx=2000)
+    g = GpuCase(c)
+    g.write_cache()
+    a = bits(g.attention())
+    b = bits(g.attention(force_chunked=True))
+    assert np.array_equal(a, b)
+
+
+def test_gqa_matches_mha_on_duplicated_kv_heads():
+    c = W.head_sweep(2, num_kv_heads=8, batch=4, ctx_len=300)
+    g = GpuCase(c)
+    g.write_cache()
+    o_gqa = bits(g.attention())
+    G = c.num_heads // c.num_kv_heads
+    kc = g.k_cache.repeat_interleave(G, dim=1).contiguous()
+    vc = g.v_cache.repeat_interleave(G, dim=1).contiguous()
+    ws = g.pa.alloc_workspace(g.pa.paged_attn_workspace_bytes(
+        c.num_seqs, c.num_heads, c.num_heads, c.head_dim, c.max_blocks_per_seq,
+        c.block_size, 0), g.q.device)
+    o_mha = bits(g.pa.paged_attn_decode(g.q, kc, vc, g.block_tables, g.context_lens, c.scale,
+                                        workspace=ws))
+    a = oracle.from_bits(o_gqa, c.dtype)
+    b = oracle.from_bits(o_mha, c.dtype)
+    assert np.max(np.abs(a - b)) <= 2 ** -7
+
+
+def test_repeated_calls_reuse_the_workspace():
+    c = _small_mixed(9)
+    g = GpuCase(c)
+    g.write_cache()
+    a = bits(g.attention())
+    for _ in range(3):
+        assert np.array_equal(a, bits(g.attention()))
+
+
+# ---------------------------------------------------------------- device checks
+def test_bad_block_id_is_flagged_not_read():
+    c = W.llama8b_decode(7, batch=4, max_ctx=300)
+    c.block_tables = c.block_tables.copy()
+    c.block_tables[1, 0] = c.num_blocks + 1000
+    g = GpuCase(c)
+    g.write_cache()
+    out = g.attention()
+    torch.cuda.synchronize()
+    assert g.status() & g.pa.PA_DEV_BAD_BLOCK_ID
+    assert np.all(np.isfinite(oracle.from_bits(bits(out), c.dtype)))
+
+
+def test_bad_slot_is_flagged_and_skipped():
+    c = W.tiny_gqa_decode(1)
+    g = GpuCase(c)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sm = g.slot_mapping.clone()
+    sm[0] = c.num_blocks * c.block_size + 3
+    before = bits(g.k_cache)
+    g.pa.reshape_and_cache(g.k_new, g.v_new, g.k_cache, g.v_cache, sm, status_word=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & g.pa.PA_DEV_BAD_SLOT
+    after = bits(g.k_cache)
+    kref = before.copy()
+    vdummy = bits(g.v_cache).copy()
+    keep = np.ones(len(c.slot_mapping), bool)
+    keep[0] = False
+    sm_h = c.slot_mapping.copy()
+    sm_h[0] = -1
+    oracle.reshape_and_cache(c.k_new, c.v_new, kref, vdummy, sm_h)
+    assert np.array_equal(after, kref)
+
+
+def test_bad_lengths_are_flagged():
+    c = _small_mixed(10)
+    c.context_lens = c.context_lens.copy()
+    i = int(np.argmax(c.query_lens))
+    c.context_lens[i] = c.query_lens[i] - 1    # qlen > ctx
+    g = GpuCase(c)
+    g.write_cache()
+    g.attention()
+    torch.cuda.synchronize()
+    assert g.status() & g.pa.PA_DEV_BAD_LENGTHS

@@ -344,6 +344,26 @@ def test_empty_context_and_empty_query():
     np.testing.assert_allclose(o, _brute_force(c), atol=1e-12)
 
 
+def test_decode_row_without_keys_is_zero():
+    c = _small_case(seed=17, B=2, Hq=4, Hkv=2, D=8, bs=4, ctx=np.array([5, 3]))
+    kc, vc = c.k_cache.copy(), c.v_cache.copy()
+    oracle.reshape_and_cache(c.k_new, c.v_new, kc, vc, c.slot_mapping)
+    ctx = c.context_lens.copy()
+    ctx[0] = 0
+    o, ob = oracle.paged_attention(c.q, kc, vc, c.block_tables, c.cu_query_lens, ctx,
+                                   c.scale, 2, c.dtype)
+    assert not o[0].any() and not ob[0].any()
+    o_ref, _ = oracle.paged_attention(c.q, kc, vc, c.block_tables, c.cu_query_lens,
+                                      c.context_lens, c.scale, 2, c.dtype)
+    assert np.array_equal(o[1], o_ref[1])
+    # a query chunk longer than a non-empty context is still an error
+    ctx[0] = 1
+    cu = np.array([0, 2, 3], np.int32)
+    q2 = np.concatenate([c.q[:1], c.q], 0)
+    with pytest.raises(ValueError):
+        oracle.paged_attention(q2, kc, vc, c.block_tables, cu, ctx, c.scale, 2, c.dtype)
+
+
 def test_bad_block_id_is_an_error():
     c = _small_case(seed=15, B=1, Hq=2, Hkv=1, D=8, bs=4, ctx=np.array([6]))
     bt = c.block_tables.copy()
