@@ -208,5 +208,8 @@ def pa_read_device_status(workspace: torch.Tensor, clear: bool = False, stream=N
 def pa_profile_next_call(start_event, stop_event) -> None:
     """Record two torch.cuda.Event objects around the attention kernels of
     the next call on this thread (see include/paged_attn.h)."""
+    for ev in (start_event, stop_event):
+        if not ev.cuda_event:  # torch creates the CUDA event on first record
+            ev.record()
     _lib.pa_profile_next_call(ctypes.c_void_p(start_event.cuda_event),
                               ctypes.c_void_p(stop_event.cuda_event))
