@@ -178,6 +178,44 @@ PA_API int pa_read_device_status(const void* workspace, int clear, uint32_t* fla
                           pa_stream_t stream);
 
 /*
+ * paged_attn_decode_noalloc -- paged_attn_decode without a caller workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot obtain device scratch memory at all (a runtime whose allocator
+ * has already reserved nearly all of HBM for its KV-cache pool and forbids
+ * further allocations, a plugin host that passes kernels only their input
+ * and output tensors, a C program with no device-memory manager).  It runs
+ * the same kernels as paged_attn_decode, with the workspace taken from a
+ * 32 MiB array that the library holds in device memory on every GPU that
+ * loads it, until the process exits.  Arguments and results are those of
+ * paged_attn_decode; q, caches, tables and out are still the caller's.
+ *
+ * Limits and rules:
+ *  - a problem whose paged_attn_workspace_bytes() exceeds 32 MiB returns
+ *    PA_ERR_WORKSPACE (pass a smaller num_splits, or split the batch);
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture;
+ *  - all calls share the one array and each call's work-list kernel
+ *    rewrites what the next kernels read, so nothing needs clearing, but
+ *    calls that overlap on the GPU (other streams, other host threads) race
+ *    on it and must be serialised by the caller;
+ *  - device status bits of these calls land in the shared array and are not
+ *    readable through pa_read_device_status.
+ * It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+PA_API int paged_attn_decode_noalloc(const void* q, const void* k_cache,
+                                     const void* v_cache,
+                                     const int32_t* block_tables,
+                                     int max_blocks_per_seq,
+                                     const int32_t* context_lens, float scale,
+                                     int num_seqs, int num_heads,
+                                     int num_kv_heads, int head_dim,
+                                     int block_size, int num_blocks, int dtype,
+                                     int num_splits, void* out,
+                                     pa_stream_t stream);
+
+/*
  * Measurement hook.  The next attention call made on this thread records
  * `start_event` on its stream just before its first attention kernel
  * (prefill or decode) and `stop_event` just after its last one, so the

@@ -57,13 +57,16 @@ _lib.paged_attn_chunked_prefill.restype = _I
 _lib.pa_read_device_status.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.pa_read_device_status.restype = _I
 
+_lib.paged_attn_decode_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _F, _I, _I, _I, _I, _I,
+                                           _I, _I, _I, _P, _P]
+_lib.paged_attn_decode_noalloc.restype = _I
 _lib.pa_profile_next_call.argtypes = [_P, _P]
 _lib.pa_profile_next_call.restype = None
 
 EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_launch_count", "reshape_and_cache",
             "paged_attn_workspace_bytes", "paged_attn_decode",
             "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
-            "pa_read_device_status"]
+            "pa_read_device_status", "paged_attn_decode_noalloc"]
 
 
 class PagedAttnError(RuntimeError):
