@@ -131,7 +131,7 @@ PA_API size_t paged_attn_workspace_bytes(int num_seqs, int num_heads,
  * blocks covers blocks [s * c, (s + 1) * c), c = ceil(nb / S)); each split
  * gives a partial output and its log-sum-exp, merged by a log-sum-exp
  * combine.  num_splits = 0 picks S per sequence (256-token splits, at most
- * 64).  scale multiplies q . k before the softmax (base e).
+ * 64).  scale (> 0) multiplies q . k before the softmax (base e).
  */
 PA_API int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, int max_blocks_per_seq,

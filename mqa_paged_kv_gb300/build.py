@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpaged_attn.so")
 
-SOURCES = ["api.cu", "schedule.cu", "reshape_and_cache.cu", "decode.cu", "prefill.cu",
+SOURCES = ["api.cu", "schedule.cu", "reshape_and_cache.cu", "decode.cu", "prefill_tc.cu",
            "static_scratch.cu"]
 HEADERS = ["pa_common.cuh", "pa_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -127,7 +127,7 @@ int check_common(const void* q, const void* k_cache, const void* v_cache,
     return PA_ERR_SHAPE;
   if (num_heads / num_kv_heads > 64) return PA_ERR_SHAPE;
   if (num_splits < 0 || num_splits > kMaxSplits) return PA_ERR_SHAPE;
-  if (!isfinite(scale)) return PA_ERR_SHAPE;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;  // softmax scale > 0
   if (num_seqs == 0) return PA_OK;
   if (max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_SHAPE;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (int64_t{1} << 30))
@@ -140,10 +140,11 @@ int check_common(const void* q, const void* k_cache, const void* v_cache,
   return PA_OK;
 }
 
-WsLayout decode_layout(int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
-                       int block_size, int num_splits) {
+WsLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                       int max_blocks_per_seq, int block_size, int num_splits) {
   const int64_t pairs =
       static_cast<int64_t>(num_seqs) * max_splits_per_seq(max_blocks_per_seq, block_size, num_splits);
+  (void)num_kv_heads;
   return workspace_layout(num_seqs, num_heads, head_dim, pairs, 0);
 }
 
@@ -228,9 +229,10 @@ int reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache
 
 size_t paged_attn_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                   int max_blocks_per_seq, int block_size, int num_splits) {
-  (void)num_kv_heads;
-  if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0) return 0;
-  return decode_layout(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size, num_splits)
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+    return 0;
+  return decode_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                       block_size, num_splits)
       .total;
 }
 
@@ -245,8 +247,8 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                         scale, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                         num_blocks, dtype, num_splits, out);
   if (rc != PA_OK || num_seqs == 0) return rc;
-  const WsLayout L =
-      decode_layout(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size, num_splits);
+  const WsLayout L = decode_layout(num_seqs, num_heads, num_kv_heads, head_dim,
+                                   max_blocks_per_seq, block_size, num_splits);
   if ((rc = check_workspace(workspace, workspace_bytes, L)) != PA_OK) return rc;
   DeviceInfo dev;
   if ((rc = current_device(dev)) != PA_OK) return rc;
@@ -295,14 +297,6 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   dp.num_blocks = num_blocks;
   dp.scale_log2 = scale * 1.4426950408889634f;
 
-  CombineParams cp;
-  cp.seq_info = pp.seq_info;
-  cp.part_o = dp.part_o;
-  cp.part_lse = dp.part_lse;
-  cp.out = out;
-  cp.num_seqs = num_seqs;
-  cp.num_heads = num_heads;
-  cp.head_dim = head_dim;
 
   const ProfileScope prof(st);
   int n = 0, r;
@@ -313,7 +307,15 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   n += r;
   prof.end();
   if (num_splits != 1) {
-    if ((r = launch_combine(cp, bf16, st)) < 0) return PA_ERR_CUDA;
+    CombineParams cp;
+    cp.seq_info = pp.seq_info;
+    cp.part_o = dp.part_o;
+    cp.part_lse = dp.part_lse;
+    cp.out = out;
+    cp.num_seqs = num_seqs;
+    cp.num_heads = num_heads;
+    cp.head_dim = head_dim;
+    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return PA_ERR_CUDA;
     n += r;
   }
   return finish(n);
@@ -415,14 +417,6 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   dp.num_blocks = num_blocks;
   dp.scale_log2 = fp.scale_log2;
 
-  CombineParams cp;
-  cp.seq_info = pp.seq_info;
-  cp.part_o = dp.part_o;
-  cp.part_lse = dp.part_lse;
-  cp.out = out;
-  cp.num_seqs = num_seqs;
-  cp.num_heads = num_heads;
-  cp.head_dim = head_dim;
 
   const ProfileScope prof(st);
   int n = 0, r;
@@ -430,8 +424,8 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   n += r;
   prof.begin();
   if (max_query_len > 1) {
-    if ((r = launch_prefill(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
-                            dev.num_sms)) < 0)
+    if ((r = launch_prefill_tc(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
+                               dev.num_sms)) < 0)
       return PA_ERR_CUDA;
     n += r;
   }
@@ -439,7 +433,15 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   n += r;
   prof.end();
   if (num_splits != 1) {
-    if ((r = launch_combine(cp, bf16, st)) < 0) return PA_ERR_CUDA;
+    CombineParams cp;
+    cp.seq_info = pp.seq_info;
+    cp.part_o = dp.part_o;
+    cp.part_lse = dp.part_lse;
+    cp.out = out;
+    cp.num_seqs = num_seqs;
+    cp.num_heads = num_heads;
+    cp.head_dim = head_dim;
+    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return PA_ERR_CUDA;
     n += r;
   }
   return finish(n);

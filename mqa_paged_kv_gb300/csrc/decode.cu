@@ -20,7 +20,9 @@
 //    P^T is turned into the B operand of the second MMA with movmatrix;
 //  * online softmax in base 2 with fp32 running max / sum per head column;
 //  * items that cover a whole sequence write the output row; split items
-//    write an fp32 partial and its log-sum-exp, merged by combine_kernel.
+//    write an fp32 partial and its log-sum-exp, merged by combine_kernel,
+//    which is launched as a programmatic dependent of this kernel so that
+//    it is resident and waiting when the last item finishes.
 #include "pa_kernels.cuh"
 
 namespace pa {
@@ -106,6 +108,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
   fence_proxy_async();
   __syncthreads();
+  griddep_wait();  // the work list is written by the preceding kernel
+  griddep_launch_dependents();  // let the split combine become resident
 
   const uint32_t num_items = p.hdr->decode_items;
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
@@ -430,43 +434,78 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
-// Merge the split partials of each decode sequence:
+// Merge the split partials of each decode sequence (one CTA per sequence,
+// one warp per query head):
 //   M = max_s lse_s, w_s = 2^(lse_s - M), out = sum_s w_s o_s / sum_s w_s,
-// with lse kept in base 2 and splits of lse = -inf weighted 0.
-template <bool kBF16>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
+// with lse in base 2 and splits of lse = -inf weighted 0.  Latency-bound by
+// design: all loads of a head are issued before any is used.
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(1024) combine_kernel(const CombineParams p) {
+  griddep_wait();  // partials are written by the decode kernel
   const int b = blockIdx.x;
   const SeqInfo si = p.seq_info[b];
   if (si.qlen != 1 || si.nsplit <= 1) return;
-  const int Hq = p.num_heads, D = p.head_dim, S = si.nsplit;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int Hq = p.num_heads, S = si.nsplit;
+  constexpr int kV = D / 32;  // floats per lane
   const float* lse = p.part_lse + static_cast<int64_t>(si.split_offset) * Hq;
   const float* po = p.part_o + static_cast<int64_t>(si.split_offset) * Hq * D;
   uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(si.tok) * Hq * D;
-  const int per_head = D / 4;
-  for (int i = threadIdx.x; i < Hq * per_head; i += blockDim.x) {
-    const int h = i / per_head, d4 = i - h * per_head;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, lse[s * Hq + h]);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, wsum = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float ls = lse[s * Hq + h];
-        if (ls == -INFINITY) continue;
-        const float w = ex2(ls - M);
-        const float4 v =
-            reinterpret_cast<const float4*>(po + (static_cast<int64_t>(s) * Hq + h) * D)[d4];
-        wsum += w;
-        a0 += w * v.x;
-        a1 += w * v.y;
-        a2 += w * v.z;
-        a3 += w * v.w;
+  for (int h = warp; h < Hq; h += nwarps) {
+    const float la = lane < S ? __ldcg(lse + static_cast<int64_t>(lane) * Hq + h) : -INFINITY;
+    const float lb = lane + 32 < S ? __ldcg(lse + static_cast<int64_t>(lane + 32) * Hq + h)
+                                   : -INFINITY;
+    float M = fmaxf(la, lb);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float wa = (M == -INFINITY || la == -INFINITY) ? 0.f : ex2(la - M);
+    const float wb = (M == -INFINITY || lb == -INFINITY) ? 0.f : ex2(lb - M);
+    float W = wa + wb;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    float acc[kV];
+#pragma unroll
+    for (int i = 0; i < kV; ++i) acc[i] = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float v[8][kV];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sp = s0 + j;
+        if (sp < S) {
+          const float* src = po + (static_cast<int64_t>(sp) * Hq + h) * D + lane * kV;
+          if constexpr (kV == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            v[j][0] = t.x; v[j][1] = t.y;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sp = s0 + j;
+        const float w = __shfl_sync(0xffffffffu, sp < 32 ? wa : wb, sp & 31);
+        if (sp < S) {
+#pragma unroll
+          for (int i = 0; i < kV; ++i) acc[i] += w * v[j][i];
+        }
       }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2 o;
-    o.x = pack2<kBF16>(a0 * inv, a1 * inv);
-    o.y = pack2<kBF16>(a2 * inv, a3 * inv);
-    reinterpret_cast<uint2*>(out + h * D)[d4] = o;
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    uint32_t packed[kV / 2];
+#pragma unroll
+    for (int i = 0; i < kV / 2; ++i) packed[i] = pack2<kBF16>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    uint16_t* dst = out + static_cast<int64_t>(h) * D + lane * kV;
+    if constexpr (kV == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    }
   }
 }
 
@@ -494,8 +533,17 @@ int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
       return -1;
     configured = dev;
   }
-  kern<<<num_sms, NW * 32, S::kBytes, stream>>>(tmk, tmv, p);
-  return 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = S::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, p) == cudaSuccess ? 1 : -1;
 }
 
 template <bool kBF16, int D>
@@ -510,6 +558,28 @@ int launch_decode_d(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
 
 }  // namespace
 
+int launch_combine(const CombineParams& p, bool bf16, int head_dim, cudaStream_t stream) {
+  if (p.num_seqs <= 0) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_seqs);
+  cfg.blockDim = dim3(32 * (p.num_heads < 32 ? p.num_heads : 32));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (bf16)
+    e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_kernel<true, 64>, p)
+                       : cudaLaunchKernelEx(&cfg, combine_kernel<true, 128>, p);
+  else
+    e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_kernel<false, 64>, p)
+                       : cudaLaunchKernelEx(&cfg, combine_kernel<false, 128>, p);
+  return e == cudaSuccess ? 1 : -1;
+}
+
 int launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                   bool bf16, int head_dim, cudaStream_t stream, int num_sms) {
   if (bf16) {
@@ -518,15 +588,6 @@ int launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodePa
   }
   return head_dim == 64 ? launch_decode_d<false, 64>(tmk, tmv, p, stream, num_sms)
                         : launch_decode_d<false, 128>(tmk, tmv, p, stream, num_sms);
-}
-
-int launch_combine(const CombineParams& p, bool bf16, cudaStream_t stream) {
-  if (p.num_seqs <= 0) return 0;
-  if (bf16)
-    combine_kernel<true><<<p.num_seqs, 256, 0, stream>>>(p);
-  else
-    combine_kernel<false><<<p.num_seqs, 256, 0, stream>>>(p);
-  return 1;
 }
 
 }  // namespace pa

@@ -15,7 +15,7 @@ namespace pa {
 constexpr int kKeyTile = 16;          // keys per decode pipeline stage
 constexpr int kAutoSplitTokens = 256; // automatic split length (tokens)
 constexpr int kMaxSplits = 64;        // splits per sequence, at most
-constexpr int kPrefillRows = 64;      // (token, head) rows per prefill tile
+constexpr int kPrefillRows = 128;     // (token, head) rows per prefill tile
 constexpr int kPrefillKeys = 64;      // keys per prefill pipeline stage
 
 // ------------------------------------------------------------------ records
@@ -43,10 +43,10 @@ struct SeqInfo {
 // A decode (sequence, split) pair; item = pair * Hkv + kv head.
 struct DecPair {
   int32_t b;
-  int32_t tok;        // query / output row
-  int32_t key_begin;  // first key (multiple of the block size)
-  int32_t key_end;    // one past the last key
-  int32_t part_idx;   // partial slot, or -1 when the split is the whole sequence
+  int32_t tok;         // query / output row
+  int32_t key_begin;   // first key (multiple of the block size)
+  int32_t key_end;     // one past the last key
+  int32_t part_idx;    // partial slot, or -1 when the split is the whole sequence
   int32_t pad[3];
 };
 
@@ -124,6 +124,7 @@ struct DecodeParams {
   float* part_lse;
   const DecPair* pairs;
   WsHeader* hdr;
+  uint32_t* done;
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks;
   float scale_log2;  // scale * log2(e)
 };
@@ -158,10 +159,10 @@ int launch_prepare(const PrepareParams& p, bool bf16, cudaStream_t stream);
 int launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                   bool bf16, int head_dim, cudaStream_t stream, int num_sms);
 
-int launch_combine(const CombineParams& p, bool bf16, cudaStream_t stream);
+int launch_combine(const CombineParams& p, bool bf16, int head_dim, cudaStream_t stream);
 
-int launch_prefill(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
-                   const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
-                   cudaStream_t stream, int num_sms);
+int launch_prefill_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                      const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
+                      cudaStream_t stream, int num_sms);
 
 }  // namespace pa

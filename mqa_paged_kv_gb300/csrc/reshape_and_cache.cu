@@ -13,6 +13,8 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
     int num_kv_heads, int chunks_per_row /* D * 2 / 16 */, int block_size, int64_t num_slots,
     uint32_t* status) {
+  griddep_wait();  // k, v and the slots may come from the previous kernel
+  griddep_launch_dependents();
   const int64_t chunks_per_token = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
   const int64_t total = num_tokens * chunks_per_token;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -49,11 +51,21 @@ int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* 
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
   if (blocks > cap) blocks = cap;
-  reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, num_tokens, num_kv_heads, chunks_per_row,
-      block_size, static_cast<int64_t>(num_blocks) * block_size, status);
-  return 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, reshape_and_cache_kernel, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
+      static_cast<int64_t>(num_tokens), num_kv_heads, chunks_per_row, block_size,
+      static_cast<int64_t>(num_blocks) * block_size, status);
+  return e == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace pa

@@ -4,12 +4,19 @@
 // reads device lengths.  Both lists are bucket-sorted longest-first, which
 // lets dynamic hand-out finish with the short items (longest-processing-time
 // order).
+//
+// Latency matters more than throughput here (it sits on the critical path of
+// every call): scans are warp-shuffle scans, and the attention kernel is
+// launched as a programmatic dependent of this one, so its prologue overlaps
+// this kernel.
 #include "pa_kernels.cuh"
 
 namespace pa {
 
 namespace {
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+static_assert(kWarps <= 32, "one warp scans the warp totals");
 constexpr int kDecBuckets = 128;  // by 16-key stages, clamped
 constexpr int kPfBuckets = 256;   // by 64-key stages, clamped
 
@@ -39,21 +46,19 @@ __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
     s.qlen = 0;
     return s;
   }
-  if (ctx == 0) return s;  // no key: the query rows are zero (written in pass 2)
+  if (ctx == 0) return s;  // no key: the query rows are zero (written below)
   if (s.qlen == 1) {
     const int nb = (ctx + p.block_size - 1) / p.block_size;
-    if (nb > 0) {
-      int chunk;
-      if (p.num_splits > 0) {
-        chunk = (nb + p.num_splits - 1) / p.num_splits;
-      } else {
-        const int auto_chunk = (kAutoSplitTokens + p.block_size - 1) / p.block_size;
-        const int cap_chunk = (nb + kMaxSplits - 1) / kMaxSplits;
-        chunk = auto_chunk > cap_chunk ? auto_chunk : cap_chunk;
-      }
-      s.nsplit = (nb + chunk - 1) / chunk;
-      s.chunk_keys = chunk * p.block_size;
+    int chunk;
+    if (p.num_splits > 0) {
+      chunk = (nb + p.num_splits - 1) / p.num_splits;
+    } else {
+      const int auto_chunk = (kAutoSplitTokens + p.block_size - 1) / p.block_size;
+      const int cap_chunk = (nb + kMaxSplits - 1) / kMaxSplits;
+      chunk = auto_chunk > cap_chunk ? auto_chunk : cap_chunk;
     }
+    s.nsplit = (nb + chunk - 1) / chunk;
+    s.chunk_keys = chunk * p.block_size;
   } else if (s.qlen > 1) {
     s.ntile = (s.qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
   }
@@ -61,36 +66,72 @@ __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
 }
 
 __device__ __forceinline__ int dec_bucket(int nkeys) {
-  int st = (nkeys + kKeyTile - 1) / kKeyTile;
+  const int st = (nkeys + kKeyTile - 1) / kKeyTile;
   return st >= kDecBuckets ? kDecBuckets - 1 : st;
 }
 
 __device__ __forceinline__ int pf_bucket(int kvlen) {
-  int st = (kvlen + kPrefillKeys - 1) / kPrefillKeys;
+  const int st = (kvlen + kPrefillKeys - 1) / kPrefillKeys;
   return st >= kPfBuckets ? kPfBuckets - 1 : st;
 }
 
-// Exclusive scan over the block; returns the block total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int& excl) {
-  const int tid = threadIdx.x;
-  scratch[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < kThreads; off <<= 1) {
-    int t = tid >= off ? scratch[tid - off] : 0;
-    __syncthreads();
-    scratch[tid] += t;
-    __syncthreads();
+// Lanes of the warp that hold the same bucket add their counts together: the
+// group's first lane reserves the group total with one shared-memory atomic,
+// and each lane gets its own start inside that range.  (Hundreds of splits
+// land in the same bucket; one atomic each would serialise them.)
+__device__ __forceinline__ int warp_aggregated_add(int* counters, int bucket, int count) {
+  const int lane = threadIdx.x & 31;
+  const unsigned grp = __match_any_sync(0xffffffffu, bucket);
+  int before = 0, total = 0;
+#pragma unroll
+  for (int src = 0; src < 32; ++src) {
+    const int c = __shfl_sync(0xffffffffu, count, src);
+    if ((grp >> src) & 1u) {
+      total += c;
+      if (src < lane) before += c;
+    }
   }
-  const int incl = scratch[tid];
-  const int total = scratch[kThreads - 1];
+  const int leader = __ffs(grp) - 1;
+  int base = 0;
+  if (lane == leader && total > 0) base = atomicAdd(&counters[bucket], total);
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + before;
+}
+
+// Exclusive scan of one int per thread over the CTA; returns the total.
+__device__ __forceinline__ int block_scan(int v, int* warp_sums, int& excl) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
-  excl = incl - v;
+  if (warp == 0) {
+    int w = lane < kWarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    if (lane < kWarps) warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = warp == 0 ? 0 : warp_sums[warp - 1];
+  const int total = warp_sums[kWarps - 1];
+  __syncthreads();
+  excl = before + x - v;
   return total;
 }
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
-  __shared__ int scan[kThreads];
+  griddep_launch_dependents();  // the attention kernel may start its prologue
+  griddep_wait();               // lengths may come from the previous kernel
+
+  __shared__ int warp_sums[kWarps];
   __shared__ int dec_cnt[kDecBuckets];
   __shared__ int pf_cnt[kPfBuckets];
   const int tid = threadIdx.x;
@@ -105,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     const int b = base + tid;
     const SeqPlan s = plan_seq(p, b);
     int excl;
-    const int tot = block_exclusive_scan(s.nsplit, scan, excl);
+    const int tot = block_scan(s.nsplit, warp_sums, excl);
     if (s.bad) Status::raise(&p.hdr->status, PA_DEV_BAD_LENGTHS);
     if (b < p.num_seqs) {
       SeqInfo si;
@@ -114,76 +155,76 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
       si.tok = s.tok;
       si.qlen = s.qlen;
       p.seq_info[b] = si;
-      for (int sp = 0; sp < s.nsplit; ++sp) {
-        const int k0 = sp * s.chunk_keys;
-        int k1 = k0 + s.chunk_keys;
-        if (k1 > s.ctx) k1 = s.ctx;
-        atomicAdd(&dec_cnt[dec_bucket(k1 - k0)], 1);
-      }
       for (int t = 0; t < s.ntile; ++t) {
-        int ntok = s.qlen - t * p.tokens_per_tile;
-        if (ntok > p.tokens_per_tile) ntok = p.tokens_per_tile;
+        const int ntok = min(s.qlen - t * p.tokens_per_tile, p.tokens_per_tile);
         const int pos0 = s.ctx - s.qlen + t * p.tokens_per_tile;
         atomicAdd(&pf_cnt[pf_bucket(pos0 + ntok)], 1);
       }
     }
+    // Decode splits: all but the last have the full chunk length.
+    {
+      const int nfull = s.nsplit > 0 ? s.nsplit - 1 : 0;
+      const int tail = s.nsplit > 0 ? s.ctx - nfull * s.chunk_keys : 0;
+      warp_aggregated_add(dec_cnt, dec_bucket(s.chunk_keys), nfull);
+      warp_aggregated_add(dec_cnt, dec_bucket(tail), s.nsplit > 0 ? 1 : 0);
+    }
     int tex;
-    tile_total += block_exclusive_scan(s.ntile, scan, tex);
+    tile_total += block_scan(s.ntile, warp_sums, tex);
     carry += tot;
   }
   __syncthreads();
 
-  // Bucket starts, longest first.
-  if (tid == 0) {
-    int acc = 0;
-    for (int k = kDecBuckets - 1; k >= 0; --k) {
-      const int c = dec_cnt[k];
-      dec_cnt[k] = acc;
-      acc += c;
-    }
-    acc = 0;
-    for (int k = kPfBuckets - 1; k >= 0; --k) {
-      const int c = pf_cnt[k];
-      pf_cnt[k] = acc;
-      acc += c;
-    }
+  // Bucket starts, longest first: scan the reversed histograms.
+  {
+    const int k = kDecBuckets - 1 - tid;
+    const int v = (tid < kDecBuckets) ? dec_cnt[k] : 0;
+    int excl;
+    block_scan(v, warp_sums, excl);
+    if (tid < kDecBuckets) dec_cnt[k] = excl;
+  }
+  {
+    const int k = kPfBuckets - 1 - tid;
+    const int v = (tid < kPfBuckets) ? pf_cnt[k] : 0;
+    int excl;
+    block_scan(v, warp_sums, excl);
+    if (tid < kPfBuckets) pf_cnt[k] = excl;
   }
   __syncthreads();
 
-  // Pass 2: emit the sorted lists.
+  // Pass 2: emit the sorted lists and zero the rows of key-less sequences.
   for (int base = 0; base < p.num_seqs; base += kThreads) {
     const int b = base + tid;
+    const SeqPlan s = plan_seq(p, b);  // all lanes take part in the warp aggregation
+    const int nfull = s.nsplit > 0 ? s.nsplit - 1 : 0;
+    const int tail = s.nsplit > 0 ? s.ctx - nfull * s.chunk_keys : 0;
+    const int pos_full = warp_aggregated_add(dec_cnt, dec_bucket(s.chunk_keys), nfull);
+    const int pos_tail = warp_aggregated_add(dec_cnt, dec_bucket(tail), s.nsplit > 0 ? 1 : 0);
     if (b >= p.num_seqs) continue;
-    const SeqPlan s = plan_seq(p, b);
     const int split_offset = p.seq_info[b].split_offset;
     for (int sp = 0; sp < s.nsplit; ++sp) {
       DecPair d;
       d.b = b;
       d.tok = s.tok;
       d.key_begin = sp * s.chunk_keys;
-      d.key_end = d.key_begin + s.chunk_keys;
-      if (d.key_end > s.ctx) d.key_end = s.ctx;
+      d.key_end = min(d.key_begin + s.chunk_keys, s.ctx);
       d.part_idx = s.nsplit > 1 ? split_offset + sp : -1;
       d.pad[0] = d.pad[1] = d.pad[2] = 0;
-      const int pos = atomicAdd(&dec_cnt[dec_bucket(d.key_end - d.key_begin)], 1);
-      p.pairs[pos] = d;
+      p.pairs[sp < nfull ? pos_full + sp : pos_tail] = d;
     }
     for (int t = 0; t < s.ntile; ++t) {
       PfTile tl;
       tl.b = b;
       tl.tok0 = s.tok + t * p.tokens_per_tile;
-      tl.ntok = s.qlen - t * p.tokens_per_tile;
-      if (tl.ntok > p.tokens_per_tile) tl.ntok = p.tokens_per_tile;
+      tl.ntok = min(s.qlen - t * p.tokens_per_tile, p.tokens_per_tile);
       tl.pos0 = s.ctx - s.qlen + t * p.tokens_per_tile;
       const int pos = atomicAdd(&pf_cnt[pf_bucket(tl.pos0 + tl.ntok)], 1);
       p.tiles[pos] = tl;
     }
-    // Query rows of a sequence with no key: zero output rows.
     if (s.ctx == 0 && s.qlen > 0 && p.out) {
-      const int64_t n = static_cast<int64_t>(p.num_heads) * p.head_dim * s.qlen;
-      uint16_t* o = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(s.tok) * p.num_heads *
-                                                        p.head_dim;
-      for (int64_t i = 0; i < n; ++i) o[i] = 0;
+      const int64_t n = static_cast<int64_t>(p.num_heads) * p.head_dim * s.qlen / 8;
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                          static_cast<int64_t>(s.tok) * p.num_heads * p.head_dim);
+      for (int64_t i = 0; i < n; ++i) o[i] = make_uint4(0, 0, 0, 0);
     }
   }
 
@@ -199,8 +240,17 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
 }
 
 int launch_prepare(const PrepareParams& p, bool /*bf16*/, cudaStream_t stream) {
-  prepare_kernel<<<1, kThreads, 0, stream>>>(p);
-  return 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prepare_kernel, p) == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace pa
