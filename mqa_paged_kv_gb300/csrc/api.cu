@@ -361,7 +361,8 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   CUtensorMap tmk, tmv, tmq;
   if ((rc = encode_cache_map(&tmk, k_cache, rows, head_dim)) != PA_OK) return rc;
   if ((rc = encode_cache_map(&tmv, v_cache, rows, head_dim)) != PA_OK) return rc;
-  if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ)) != PA_OK)
+  if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
+      PA_OK)
     return rc;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -15,7 +15,7 @@ namespace pa {
 constexpr int kKeyTile = 16;          // keys per decode pipeline stage
 constexpr int kAutoSplitTokens = 256; // automatic split length (tokens)
 constexpr int kMaxSplits = 64;        // splits per sequence, at most
-constexpr int kPrefillRows = 128;     // (token, head) rows per prefill tile
+constexpr int kPrefillTileRows = 128; // (token, head) rows of one MMA tile
 constexpr int kPrefillKeys = 64;      // keys per prefill pipeline stage
 
 // ------------------------------------------------------------------ records
@@ -76,9 +76,11 @@ inline int64_t max_splits_per_seq(int max_blocks_per_seq, int block_size, int nu
   return s;
 }
 
+// A prefill work item is two MMA tiles of the same sequence and KV head:
+// 2 * floor(128 / G) query tokens.
 inline int prefill_tokens_per_tile(int G) {
-  const int t = kPrefillRows / G;
-  return t < 1 ? 1 : t;
+  const int t = kPrefillTileRows / G;
+  return 2 * (t < 1 ? 1 : t);
 }
 
 inline WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int64_t max_pairs,

@@ -6,38 +6,41 @@
 // the chunk after a cached prefix) next to decode rows; vLLM issue #1880
 // ("[Performance] Use optimized kernels for MQA/GQA", opening paragraph) asks
 // that the G query heads sharing a KV head share its cache reads and do the
-// dot products on tensor cores.  A tile packs those G heads times 128 / G
+// dot products on tensor cores.  A Q tile packs those G heads times 128 / G
 // consecutive query tokens as the M = 128 rows of the MMA (row r = token * G
-// + head), so each 128-key K/V tile gathered from the cache feeds all of them
-// and the products are real 128 x 128 x 16 MMAs.
+// + head), and each CTA works on two such tiles (A: the first 128 / G
+// tokens, B: the next) of one sequence and KV head, so every 64-key K/V
+// stage gathered from the cache feeds 256 rows.
 //
 // Warp roles (one CTA per SM, persistent over a device tile list):
-//   warp 0     TMA producer: Q tile (one 3-D box per 64 columns), then the
-//              visible keys in 128-key stages, each a set of 16-key boxes
-//              gathered through the block table (two stages in flight);
-//   warp 1     MMA issuer (one thread): S = Q K^T into tensor memory, two S
-//              buffers, then O += P V, O in tensor memory;
-//   warps 2-5  softmax, one thread per row (= TMEM lane): scale, bottom-right
-//              causal mask, running max, P = 2^(x - m) rounded to the
-//              element type into shared memory (two P buffers, so the
-//              softmax of tile j overlaps QK of tile j+1 and PV of tile j-1),
-//              fp32 row sum, and the epilogue O / l.  Row maxima run over the
-//              raw scores in eight independent chains and the scale is
-//              folded into the exponent's FMA (so scale must be positive).
+//   warp 0     TMA producer: the two Q tiles (one 3-D box per 64 columns
+//              each), then the visible keys in 64-key stages through a
+//              4-deep ring; a stage is 16-key boxes gathered through the
+//              block table, one box per lane, issued by one instruction;
+//   warp 1     MMA issuer (one thread): S_t = Q_t K^T into tensor memory
+//              (two S buffers per tile), O_t += P_t V (O in tensor memory);
+//   warps 2-9  softmax, four warps per tile, one thread per row (= TMEM
+//              lane): scale, bottom-right causal mask, running max,
+//              P = 2^(x*scale - m) in the element type into shared memory,
+//              fp32 row sum, and the epilogue O / l.
 // The running max is a reference that only moves when a row max exceeds it
 // by more than 2^8 (then O and l are rescaled in place); between moves P
-// stays below 256, well inside the element type.
+// stays below 256, well inside the element type.  Row maxima run over raw
+// scores in eight independent chains and the scale is folded into the
+// exponent's FMA, so the scale must be positive.
 #include "pa_kernels.cuh"
 
 namespace pa {
 
 namespace {
 
-constexpr int kTcRows = 128;             // M: packed (token, head) rows
-constexpr int kTcKeys = 128;             // keys per stage (N of QK, K of PV)
-constexpr int kTcSub = kTcKeys / 16;     // 16-key TMA boxes per stage
-constexpr int kTcThreads = 6 * 32;
-constexpr float kRescaleThreshold = 8.f; // log2 of the largest unnormalised P
+constexpr int kTcRows = 128;              // M of one tile
+constexpr int kTcKeys = 64;               // keys per stage
+constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per stage
+constexpr int kTcStages = 4;              // K/V ring depth
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
+constexpr float kRescaleThreshold = 8.f;  // log2 of the largest unnormalised P
 
 struct TcMeta {
   int32_t tok0, ntok, pos0, kvh, nkv, done, b, pad;
@@ -46,33 +49,38 @@ struct TcMeta {
 enum : int {
   kBarQFull = 0,
   kBarQEmpty,
-  kBarKvFull,      // [2]
-  kBarKvEmpty = kBarKvFull + 2,
-  kBarSFull = kBarKvEmpty + 2,
-  kBarSEmpty = kBarSFull + 2,
-  kBarPFull = kBarSEmpty + 2,
-  kBarPvDone = kBarPFull + 2,
-  kBarOFull = kBarPvDone + 2,
-  kBarOEmpty,
-  kNumBars
+  kBarKvFull,                              // [stages]
+  kBarKvEmpty = kBarKvFull + kTcStages,    // [stages]
+  kBarSFull = kBarKvEmpty + kTcStages,     // [tile][buffer]
+  kBarSEmpty = kBarSFull + 4,              // [tile][buffer]
+  kBarPFull = kBarSEmpty + 4,              // [tile]
+  kBarPvDone = kBarPFull + 2,              // [tile]
+  kBarOFull = kBarPvDone + 2,              // [tile]
+  kBarOEmpty = kBarOFull + 2,              // [tile]
+  kNumBars = kBarOEmpty + 2
 };
 
 template <int D>
 struct TcSmem {
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kRegion = 128 * 128;  // 128 rows x 128 B, one swizzle column
-  static constexpr int kQ = kBoxes * kRegion;
-  static constexpr int kKV = kBoxes * kRegion;  // 128 keys of K (or V)
+  static constexpr int kBoxes = D / 64;            // 64-column halves
+  static constexpr int kQRegion = 128 * 128;       // 128 rows x 128 B
+  static constexpr int kQ = kBoxes * kQRegion;     // one Q tile
+  static constexpr int kKVRegion = kTcKeys * 128;  // 64 keys x 128 B
+  static constexpr int kKV = kBoxes * kKVRegion;   // 64 keys of K (or V)
   static constexpr int kStage = 2 * kKV;
-  static constexpr int kP = 2 * kRegion;        // 128 rows x 128 keys, 16-bit
-  static constexpr int kOffKV = kQ;
-  static constexpr int kOffP = kOffKV + 2 * kStage;
+  static constexpr int kP = 128 * 128;             // 128 rows x 64 keys, 16-bit
+  static constexpr int kOffKV = 2 * kQ;
+  static constexpr int kOffP = kOffKV + kTcStages * kStage;
   static constexpr int kOffBar = kOffP + 2 * kP;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
   static constexpr int kBytes = kOffTmem + 16 + 1024;
-  static constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr uint32_t kTmemCols = 512;
+  // tile t, buffer b: S at t*128 + b*64; O_t at 256 + t*128
+  static constexpr uint32_t col_s(int t, int b) {
+    return static_cast<uint32_t>(t * 128 + b * 64);
+  }
+  static constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * 128); }
 };
 
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, uint32_t* status) {
@@ -102,17 +110,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar[kBarQFull], 1);
-    mbar_init(&bar[kBarQEmpty], 1 + 4);  // MMA commit + 4 softmax warps (meta read)
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(&bar[kBarQEmpty], 1 + kTcSoftmaxWarps);  // MMA commit + meta reads
+    for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&bar[kBarKvFull + i], 1);
       mbar_init(&bar[kBarKvEmpty + i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
       mbar_init(&bar[kBarSEmpty + i], 4);
-      mbar_init(&bar[kBarPFull + i], 4);
-      mbar_init(&bar[kBarPvDone + i], 1);
     }
-    mbar_init(&bar[kBarOFull], 1);
-    mbar_init(&bar[kBarOEmpty], 4);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar[kBarPFull + t], 4);
+      mbar_init(&bar[kBarPvDone + t], 1);
+      mbar_init(&bar[kBarOFull + t], 1);
+      mbar_init(&bar[kBarOEmpty + t], 4);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
@@ -123,7 +135,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   griddep_wait();  // the tile list is written by the preceding kernel
 
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
-  const int TQ = p.tokens_per_tile;
+  const int TQ = p.tokens_per_tile / 2;  // tokens of one of the two Q tiles
   uint32_t* status = &p.hdr->status;
   const uint32_t num_items = p.hdr->prefill_items;
 
@@ -135,7 +147,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tmq);
     }
     const int oob_row = p.num_blocks * Hkv * bs;  // a box here reads zeros
-    uint32_t t_iter = 0, kv_iter = 0;
+    constexpr int nb = kTcSub * S::kBoxes;        // K boxes per stage (= V boxes)
+    static_assert(2 * nb <= 32, "one box per lane");
+    const bool is_v = lane >= nb;
+    const int box = is_v ? lane - nb : lane;
+    const int my_j = box / S::kBoxes, my_bx = box % S::kBoxes;
+    uint32_t t_iter = 0, g = 0;
     bool ok = true;
     while (ok) {
       uint32_t it = 0;
@@ -164,34 +181,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m.b = tile.b;
         m.pad = 0;
         *meta = m;
-        mbar_arrive_expect_tx(&bar[kBarQFull], static_cast<uint32_t>(S::kBoxes * 128 * G * TQ));
+        mbar_arrive_expect_tx(&bar[kBarQFull],
+                              static_cast<uint32_t>(2 * S::kBoxes * 128 * G * TQ));
 #pragma unroll
-        for (int bx = 0; bx < S::kBoxes; ++bx)
-          tma_load_3d(sq + bx * S::kRegion, &tmq, bx * 64, kvh * G, tile.tok0, &bar[kBarQFull]);
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int bx = 0; bx < S::kBoxes; ++bx)
+            tma_load_3d(sq + t * S::kQ + bx * S::kQRegion, &tmq, bx * 64, kvh * G,
+                        tile.tok0 + t * TQ, &bar[kBarQFull]);
       }
       ++t_iter;
 
-      // Physical block ids, 32 per window; the next window is loaded while
-      // the current one is in use, so no stage waits on a table read.
+      // Physical block ids, 32 per window held one per lane; the next window
+      // is loaded while the current one is in use.
       auto load_window = [&](int lblk0) -> int {
         const int lb = lblk0 + lane;
-        return (lb * bs < nkv) ? __ldg(p.block_tables + static_cast<int64_t>(tile.b) * p.mbs + lb)
-                               : -1;
+        return (lb * bs < nkv)
+                   ? __ldg(p.block_tables + static_cast<int64_t>(tile.b) * p.mbs + lb)
+                   : -1;
       };
       int ids_base = 0;
       int ids = load_window(0);
       int ids_next = load_window(32);
-      for (int kb = 0; kb < nkv; kb += kTcKeys) {
-        const int s = static_cast<int>(kv_iter & 1);
-        if (kv_iter >= 2 && !wait_or_flag(&bar[kBarKvEmpty + s], ((kv_iter >> 1) - 1) & 1, status)) {
+      int lblk = 0, off = 0;  // block and slot of the next 16-key box
+      for (int kb = 0; kb < nkv; kb += kTcKeys, ++g) {
+        const int st = static_cast<int>(g % kTcStages);
+        if (g >= kTcStages &&
+            !wait_or_flag(&bar[kBarKvEmpty + st], ((g / kTcStages) - 1) & 1, status)) {
           ok = false;
           break;
         }
-        int rows[kTcSub];
+        int my_row = oob_row;
 #pragma unroll
         for (int j = 0; j < kTcSub; ++j) {
           const int key = kb + 16 * j;
-          const int lblk = key / bs;
           if (key < nkv && lblk - ids_base >= 32) {  // windows advance in order
             ids_base += 32;
             ids = ids_next;
@@ -202,24 +225,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) Status::raise(status, PA_DEV_BAD_BLOCK_ID);
             blk = -1;
           }
-          rows[j] = (key < nkv && blk >= 0) ? (blk * Hkv + kvh) * bs + (key % bs) : oob_row;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar[kBarKvFull + s],
-                                static_cast<uint32_t>(kTcSub * 2 * S::kBoxes * 2048));
-          uint8_t* st = skv + s * S::kStage;
-#pragma unroll
-          for (int j = 0; j < kTcSub; ++j) {
-#pragma unroll
-            for (int bx = 0; bx < S::kBoxes; ++bx) {
-              tma_load_2d(st + bx * S::kRegion + j * 2048, &tmk, bx * 64, rows[j],
-                          &bar[kBarKvFull + s]);
-              tma_load_2d(st + S::kKV + bx * S::kRegion + j * 2048, &tmv, bx * 64, rows[j],
-                          &bar[kBarKvFull + s]);
-            }
+          const int row = (key < nkv && blk >= 0) ? (blk * Hkv + kvh) * bs + off : oob_row;
+          if (j == my_j) my_row = row;
+          off += 16;
+          if (off == bs) {
+            off = 0;
+            ++lblk;
           }
         }
-        ++kv_iter;
+        if (lane == 0)
+          mbar_arrive_expect_tx(&bar[kBarKvFull + st], static_cast<uint32_t>(S::kStage));
+        __syncwarp();
+        if (lane < 2 * nb) {
+          uint8_t* dst = skv + st * S::kStage + (is_v ? S::kKV : 0) + my_bx * S::kKVRegion +
+                         my_j * 2048;
+          tma_load_2d(dst, is_v ? &tmv : &tmk, my_bx * 64, my_row, &bar[kBarKvFull + st]);
+        }
       }
     }
   } else if (warp == 1) {
@@ -229,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t q_addr = smem_u32(sq);
     const uint32_t kv_addr = smem_u32(skv);
     const uint32_t p_addr = smem_u32(sp);
-    uint32_t t_iter = 0, kv_iter = 0;
+    uint32_t t_iter = 0, g0 = 0;
     bool ok = true;
     while (ok) {
       if (!wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
@@ -239,104 +260,111 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
 
       auto issue_pv = [&](int jj) -> bool {
-        const uint32_t g = kv_iter + jj;
-        const int s = static_cast<int>(g & 1);
-        if (jj == 0 && t_iter > 0 && !wait_or_flag(&bar[kBarOEmpty], (t_iter - 1) & 1, status))
-          return false;
-        if (!wait_or_flag(&bar[kBarPFull + s], (g >> 1) & 1, status)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const int keys = min(kTcKeys, m.nkv - jj * kTcKeys);
-          const int ksteps = (keys + 15) / 16;
-          const uint32_t vbase = kv_addr + s * S::kStage + S::kKV;
-          const uint32_t pbase = p_addr + s * S::kP;
-          for (int ks = 0; ks < ksteps; ++ks) {
-            const uint64_t ad = sdesc_sw128(pbase + (ks >> 2) * S::kRegion + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vbase + ks * 2048, S::kRegion, 1024);
-            umma_f16(tmem + S::kColO, ad, bd, kIdPV, (jj > 0 || ks > 0) ? 1u : 0u);
+        const uint32_t g = g0 + jj;
+        const int st = static_cast<int>(g % kTcStages);
+        const int keys = min(kTcKeys, m.nkv - jj * kTcKeys);
+        const int ksteps = (keys + 15) / 16;
+        for (int t = 0; t < 2; ++t) {
+          if (!wait_or_flag(&bar[kBarPFull + t], g & 1, status)) return false;
+          if (jj == 0 && t_iter > 0 &&
+              !wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status))
+            return false;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t vbase = kv_addr + st * S::kStage + S::kKV;
+            const uint32_t pbase = p_addr + t * S::kP;
+            for (int ks = 0; ks < ksteps; ++ks) {
+              const uint64_t ad = sdesc_sw128(pbase + ks * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(vbase + ks * 2048, S::kKVRegion, 1024);
+              umma_f16(tmem + S::col_o(t), ad, bd, kIdPV, (jj > 0 || ks > 0) ? 1u : 0u);
+            }
+            umma_commit(&bar[kBarPvDone + t]);
+            if (t == 1) umma_commit(&bar[kBarKvEmpty + st]);
+            if (jj == n - 1) umma_commit(&bar[kBarOFull + t]);
           }
-          umma_commit(&bar[kBarKvEmpty + s]);
-          umma_commit(&bar[kBarPvDone + s]);
+          __syncwarp();
         }
-        __syncwarp();
         return true;
       };
 
       for (int j = 0; j < n && ok; ++j) {
-        const uint32_t g = kv_iter + j;
-        const int s = static_cast<int>(g & 1);
-        if (!wait_or_flag(&bar[kBarKvFull + s], (g >> 1) & 1, status)) { ok = false; break; }
-        if (g >= 2 && !wait_or_flag(&bar[kBarSEmpty + s], ((g >> 1) - 1) & 1, status)) {
+        const uint32_t g = g0 + j;
+        const int st = static_cast<int>(g % kTcStages);
+        const int b = static_cast<int>(g & 1);
+        if (!wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kbase = kv_addr + s * S::kStage;
-          const uint32_t dcol = tmem + (s ? S::kColS1 : S::kColS0);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * S::kRegion + (ks & 3) * 32;
-            umma_f16(dcol, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                     kIdQK, ks > 0 ? 1u : 0u);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (g >= 2 &&
+              !wait_or_flag(&bar[kBarSEmpty + 2 * t + b], ((g >> 1) - 1) & 1, status)) {
+            ok = false;
+            break;
           }
-          umma_commit(&bar[kBarSFull + s]);
-          if (j == n - 1) umma_commit(&bar[kBarQEmpty]);
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t kbase = kv_addr + st * S::kStage;
+            const uint32_t qbase = q_addr + t * S::kQ;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              umma_f16(tmem + S::col_s(t, b),
+                       sdesc_sw128(qbase + (ks >> 2) * S::kQRegion + (ks & 3) * 32, 16, 1024),
+                       sdesc_sw128(kbase + (ks >> 2) * S::kKVRegion + (ks & 3) * 32, 16, 1024),
+                       kIdQK, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(&bar[kBarSFull + 2 * t + b]);
+            if (t == 1 && j == n - 1) umma_commit(&bar[kBarQEmpty]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (ok && j >= 1 && !issue_pv(j - 1)) ok = false;
       }
       if (!ok || !issue_pv(n - 1)) break;
-      if (lane == 0) umma_commit(&bar[kBarOFull]);
-      __syncwarp();
-      kv_iter += n;
+      g0 += n;
       ++t_iter;
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;               // TMEM lanes 32*quarter ..
+    const int t = (warp - 2) / 4;    // Q tile of this warp
+    const int quarter = warp & 3;    // TMEM lanes 32*quarter ..
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     const int rows_used = G * TQ;
-    uint32_t t_iter = 0, kv_iter = 0;
+    uint8_t* prow = sp + t * S::kP + row * 128;
+    uint32_t t_iter = 0, g0 = 0;
     while (true) {
       if (!wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
       const TcMeta m = *meta;
       __syncwarp();
       if (m.done) break;
       if (lane == 0) mbar_arrive(&bar[kBarQEmpty]);
-      const int t = row / G;
-      const bool valid = row < rows_used && t < m.ntok;
-      const int pos = m.pos0 + t;
+      const int tl = t * TQ + row / G;  // token within the pair
+      const bool valid = row < rows_used && tl < m.ntok;
+      const int pos = m.pos0 + tl;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        const uint32_t g = kv_iter + j;
-        const int s = static_cast<int>(g & 1);
-        if (!wait_or_flag(&bar[kBarSFull + s], (g >> 1) & 1, status)) { ok = false; break; }
+        const uint32_t g = g0 + j;
+        const int b = static_cast<int>(g & 1);
+        if (!wait_or_flag(&bar[kBarSFull + 2 * t + b], (g >> 1) & 1, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         float x[kTcKeys];
-        {
-          uint32_t r[kTcKeys];
-          tmem_ld128(lane_base + (s ? S::kColS1 : S::kColS0), r);
-#pragma unroll
-          for (int i = 0; i < kTcKeys; ++i) x[i] = __uint_as_float(r[i]);
-        }
+        tmem_ld64f(lane_base + S::col_s(t, b), x);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarSEmpty + s]);
+        if (lane == 0) mbar_arrive(&bar[kBarSEmpty + 2 * t + b]);
 
         const int kb = j * kTcKeys;
-        // Mask only where a key can be past this row's position or past the
-        // sequence (the tile on the diagonal and the last tile).
         const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this row
         if (__any_sync(0xffffffffu, lim < kTcKeys - 1)) {
 #pragma unroll
           for (int i = 0; i < kTcKeys; ++i)
             if (i > lim) x[i] = -INFINITY;
         }
-        // Row max over raw scores (scale > 0), eight independent chains.
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = x[e];
@@ -345,27 +373,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
                          p.scale_log2;
-        // P buffer s was last read by PV of KV tile g - 2.
-        if (g >= 2 && !wait_or_flag(&bar[kBarPvDone + s], ((g >> 1) - 1) & 1, status)) {
+        // P_t was last read (and O_t last written) by PV of stage g - 1.
+        if (g >= 1 && !wait_or_flag(&bar[kBarPvDone + t], (g - 1) & 1, status)) {
           ok = false;
           break;
         }
         const bool need = m_ref != -INFINITY && mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold PV of tile g - 1 before it is rescaled.
-          if (!wait_or_flag(&bar[kBarPvDone + ((g - 1) & 1)], ((g - 1) >> 1) & 1, status)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const float alpha = need ? ex2(m_ref - mx) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(lane_base + S::col_o(t) + c * 16, r);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + S::kColO + c * 32, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(lane_base + S::kColO + c * 32, r);
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st16(lane_base + S::col_o(t) + c * 16, r);
           }
           tmem_wait_st();
           if (need) {
@@ -376,9 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (m_ref == -INFINITY) m_ref = mx;
         const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
 
-        // P = 2^(x * scale - m) into buffer s (K-major, 128-byte swizzle:
-        // keys 0-63, then 64-127); the row sum takes the fp32 values.
-        uint8_t* prow = sp + s * S::kP + row * 128;
+        // P row (K-major, 128-byte swizzle: 64 keys = one 128-byte row).
         float rs8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
@@ -393,26 +414,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             rs8[2 * e + 1] += p1;
             w[e] = pack2<kBF16>(p0, p1);
           }
-          const int region = c >> 3, chunk = c & 7;
-          *reinterpret_cast<uint4*>(prow + region * S::kRegion + ((chunk ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
 
         // Keys past the sequence inside the last loaded 16-key box hold
         // whatever the cache slots hold: zero those V rows (P is 0 there,
-        // but 0 * NaN is not).
+        // but 0 * NaN is not).  Both tiles' warps write the same zeros.
         if (j == n - 1) {
-          const int r0 = m.nkv - kb;                      // first stale key in the stage
+          const int r0 = m.nkv - kb;
           const int r1 = min(kTcKeys, (r0 + 15) / 16 * 16);
           if (r1 > r0) {
-            if (!wait_or_flag(&bar[kBarKvFull + s], (g >> 1) & 1, status)) { ok = false; break; }
-            uint8_t* vst = skv + s * S::kStage + S::kKV;
-            const int per_row = S::kBoxes * 8;          // 16-byte chunks per key row
+            const int st = static_cast<int>(g % kTcStages);
+            if (!wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* vst = skv + st * S::kStage + S::kKV;
+            const int per_row = S::kBoxes * 8;  // 16-byte chunks per key row
             const int total = (r1 - r0) * per_row;
             for (int i = row; i < total; i += 128) {
               const int kr = r0 + i / per_row, c = i % per_row;
-              *reinterpret_cast<uint4*>(vst + (c >> 3) * S::kRegion + kr * 128 + (c & 7) * 16) =
+              *reinterpret_cast<uint4*>(vst + (c >> 3) * S::kKVRegion + kr * 128 + (c & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
           }
@@ -420,37 +444,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarPFull + s]);
+        if (lane == 0) mbar_arrive(&bar[kBarPFull + t]);
       }
       if (!ok) break;
 
-      // Epilogue: O / l for the valid rows.
-      if (!wait_or_flag(&bar[kBarOFull], t_iter & 1, status)) break;
+      // Epilogue: O_t / l for the valid rows.
+      if (!wait_or_flag(&bar[kBarOFull + t], t_iter & 1, status)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                       (static_cast<int64_t>(m.tok0 + t) * Hq + static_cast<int64_t>(m.kvh) * G +
+                       (static_cast<int64_t>(m.tok0 + tl) * Hq + static_cast<int64_t>(m.kvh) * G +
                         row % G) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_base + S::kColO + c * 32, r);
+        tmem_ld32(lane_base + S::col_o(t) + c * 32, r);
         if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 o;
-            o.x = pack2<kBF16>(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
-            o.y = pack2<kBF16>(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
-            o.z = pack2<kBF16>(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
-            o.w = pack2<kBF16>(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+            o.x = pack2<kBF16>(__uint_as_float(r[8 * q + 0]) * inv,
+                               __uint_as_float(r[8 * q + 1]) * inv);
+            o.y = pack2<kBF16>(__uint_as_float(r[8 * q + 2]) * inv,
+                               __uint_as_float(r[8 * q + 3]) * inv);
+            o.z = pack2<kBF16>(__uint_as_float(r[8 * q + 4]) * inv,
+                               __uint_as_float(r[8 * q + 5]) * inv);
+            o.w = pack2<kBF16>(__uint_as_float(r[8 * q + 6]) * inv,
+                               __uint_as_float(r[8 * q + 7]) * inv);
             reinterpret_cast<uint4*>(orow + c * 32)[q] = o;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kBarOEmpty]);
-      kv_iter += n;
+      if (lane == 0) mbar_arrive(&bar[kBarOEmpty + t]);
+      g0 += n;
       ++t_iter;
     }
   }
