@@ -47,7 +47,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode",
@@ -402,6 +402,8 @@ def run_ours(args):
 
     te, _, h2d, d2h = time_steps(step, max(3, args.steps // 2), 2, flush, e2e=True)
 
+    step_stats = {"min_ms": float(t.min()), "median_ms": float(np.median(t)),
+                  "max_ms": float(t.max()), "mean_ms": float(t.mean())}
     step_s = float(t.mean()) / 1e3
     kern_s = float(kt.mean()) / 1e3
     e2e_s = float(te.mean()) / 1e3
@@ -428,7 +430,8 @@ def run_ours(args):
         "config": dict(W.describe(case), splits=args.splits or "auto",
                        l2=f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB read sweep)",
                        parallelism="replicas" if world > 1 else "single GPU",
-                       step="reshape_and_cache + paged attention"),
+                       step="reshape_and_cache + paged attention",
+                       step_time_stats=step_stats),
         "hbm_peak_frac": value / world / peak,
         "tokens_per_s": case.total_query_tokens * world / step_s,
         "roofline": {"bound": "hbm", "kernel": main_kernel, "achieved": achieved, "peak": peak,

@@ -453,9 +453,30 @@ __global__ void __launch_bounds__(1024) combine_kernel(const CombineParams p) {
   const float* po = p.part_o + static_cast<int64_t>(si.split_offset) * Hq * D;
   uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(si.tok) * Hq * D;
   for (int h = warp; h < Hq; h += nwarps) {
+    // Issue the log-sum-exps and the first eight partial rows together.
+    auto load_part = [&](int sp, float (&dst)[kV]) {
+      const float* src = po + (static_cast<int64_t>(sp) * Hq + h) * D + lane * kV;
+      if constexpr (kV == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+        dst[0] = t.x; dst[1] = t.y; dst[2] = t.z; dst[3] = t.w;
+      } else {
+        const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+        dst[0] = t.x; dst[1] = t.y;
+      }
+    };
     const float la = lane < S ? __ldcg(lse + static_cast<int64_t>(lane) * Hq + h) : -INFINITY;
     const float lb = lane + 32 < S ? __ldcg(lse + static_cast<int64_t>(lane + 32) * Hq + h)
                                    : -INFINITY;
+    float v[8][kV];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < S) {
+        load_part(j, v[j]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+      }
+    }
     float M = fmaxf(la, lb);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -468,22 +489,15 @@ __global__ void __launch_bounds__(1024) combine_kernel(const CombineParams p) {
 #pragma unroll
     for (int i = 0; i < kV; ++i) acc[i] = 0.f;
     for (int s0 = 0; s0 < S; s0 += 8) {
-      float v[8][kV];
+      if (s0 > 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int sp = s0 + j;
-        if (sp < S) {
-          const float* src = po + (static_cast<int64_t>(sp) * Hq + h) * D + lane * kV;
-          if constexpr (kV == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+        for (int j = 0; j < 8; ++j) {
+          if (s0 + j < S) {
+            load_part(s0 + j, v[j]);
           } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-            v[j][0] = t.x; v[j][1] = t.y;
-          }
-        } else {
 #pragma unroll
-          for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+            for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+          }
         }
       }
 #pragma unroll

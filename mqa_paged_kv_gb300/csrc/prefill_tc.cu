@@ -15,14 +15,16 @@
 // Warp roles (one CTA per SM, persistent over a device tile list):
 //   warp 0     TMA producer: the two Q tiles (one 3-D box per 64 columns
 //              each), then the visible keys in 64-key stages through a
-//              4-deep ring; a stage is 16-key boxes gathered through the
+//              5-deep ring; a stage is 16-key boxes gathered through the
 //              block table, one box per lane, issued by one instruction;
 //   warp 1     MMA issuer (one thread): S_t = Q_t K^T into tensor memory
-//              (two S buffers per tile), O_t += P_t V (O in tensor memory);
+//              (two S buffers per tile), O_t += P_t V with P_t read from
+//              tensor memory (O in tensor memory);
 //   warps 2-9  softmax, four warps per tile, one thread per row (= TMEM
 //              lane): scale, bottom-right causal mask, running max,
-//              P = 2^(x*scale - m) in the element type into shared memory,
-//              fp32 row sum, and the epilogue O / l.
+//              P = 2^(x*scale - m) in the element type written back over
+//              its own S buffer in tensor memory (so shared memory holds
+//              only Q and the K/V ring), fp32 row sum, and the epilogue O / l.
 // The running max is a reference that only moves when a row max exceeds it
 // by more than 2^8 (then O and l are rescaled in place); between moves P
 // stays below 256, well inside the element type.  Row maxima run over raw
@@ -37,7 +39,7 @@ namespace {
 constexpr int kTcRows = 128;              // M of one tile
 constexpr int kTcKeys = 64;               // keys per stage
 constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per stage
-constexpr int kTcStages = 4;              // K/V ring depth
+constexpr int kTcStages = 5;              // K/V ring depth
 constexpr int kTcSoftmaxWarps = 8;
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 of the largest unnormalised P
@@ -52,10 +54,9 @@ enum : int {
   kBarKvFull,                              // [stages]
   kBarKvEmpty = kBarKvFull + kTcStages,    // [stages]
   kBarSFull = kBarKvEmpty + kTcStages,     // [tile][buffer]
-  kBarSEmpty = kBarSFull + 4,              // [tile][buffer]
-  kBarPFull = kBarSEmpty + 4,              // [tile]
-  kBarPvDone = kBarPFull + 2,              // [tile]
-  kBarOFull = kBarPvDone + 2,              // [tile]
+  kBarPFull = kBarSFull + 4,               // [tile][buffer]
+  kBarPvDone = kBarPFull + 4,              // [tile][buffer]
+  kBarOFull = kBarPvDone + 4,              // [tile]
   kBarOEmpty = kBarOFull + 2,              // [tile]
   kNumBars = kBarOEmpty + 2
 };
@@ -68,15 +69,14 @@ struct TcSmem {
   static constexpr int kKVRegion = kTcKeys * 128;  // 64 keys x 128 B
   static constexpr int kKV = kBoxes * kKVRegion;   // 64 keys of K (or V)
   static constexpr int kStage = 2 * kKV;
-  static constexpr int kP = 128 * 128;             // 128 rows x 64 keys, 16-bit
   static constexpr int kOffKV = 2 * kQ;
-  static constexpr int kOffP = kOffKV + kTcStages * kStage;
-  static constexpr int kOffBar = kOffP + 2 * kP;
+  static constexpr int kOffBar = kOffKV + kTcStages * kStage;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
   static constexpr int kBytes = kOffTmem + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // tile t, buffer b: S at t*128 + b*64; O_t at 256 + t*128
+  // tile t, buffer b: S (fp32, 64 columns) at t*128 + b*64, later P (16-bit
+  // pairs, its first 32 columns); O_t at 256 + t*128
   static constexpr uint32_t col_s(int t, int b) {
     return static_cast<uint32_t>(t * 128 + b * 64);
   }
@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sq = smem;
   uint8_t* skv = smem + S::kOffKV;
-  uint8_t* sp = smem + S::kOffP;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   TcMeta* meta = reinterpret_cast<TcMeta*>(smem + S::kOffMeta);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffTmem);
@@ -117,11 +116,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
-      mbar_init(&bar[kBarSEmpty + i], 4);
+      mbar_init(&bar[kBarPFull + i], 4);
+      mbar_init(&bar[kBarPvDone + i], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bar[kBarPFull + t], 4);
-      mbar_init(&bar[kBarPvDone + t], 1);
       mbar_init(&bar[kBarOFull + t], 1);
       mbar_init(&bar[kBarOEmpty + t], 4);
     }
@@ -249,7 +247,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t kIdPV = idesc_f16(kTcRows, D, kBF16, false, true);
     const uint32_t q_addr = smem_u32(sq);
     const uint32_t kv_addr = smem_u32(skv);
-    const uint32_t p_addr = smem_u32(sp);
     uint32_t t_iter = 0, g0 = 0;
     bool ok = true;
     while (ok) {
@@ -264,21 +261,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int st = static_cast<int>(g % kTcStages);
         const int keys = min(kTcKeys, m.nkv - jj * kTcKeys);
         const int ksteps = (keys + 15) / 16;
+        const int pb = static_cast<int>(g & 1);
         for (int t = 0; t < 2; ++t) {
-          if (!wait_or_flag(&bar[kBarPFull + t], g & 1, status)) return false;
+          if (!wait_or_flag(&bar[kBarPFull + 2 * t + pb], (g >> 1) & 1, status)) return false;
           if (jj == 0 && t_iter > 0 &&
               !wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status))
             return false;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t vbase = kv_addr + st * S::kStage + S::kKV;
-            const uint32_t pbase = p_addr + t * S::kP;
+            const uint32_t pcol = tmem + S::col_s(t, pb);
             for (int ks = 0; ks < ksteps; ++ks) {
-              const uint64_t ad = sdesc_sw128(pbase + ks * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(vbase + ks * 2048, S::kKVRegion, 1024);
-              umma_f16(tmem + S::col_o(t), ad, bd, kIdPV, (jj > 0 || ks > 0) ? 1u : 0u);
+              umma_f16_ts(tmem + S::col_o(t), pcol + ks * 8, bd, kIdPV, (jj > 0 || ks > 0) ? 1u : 0u);
             }
-            umma_commit(&bar[kBarPvDone + t]);
+            umma_commit(&bar[kBarPvDone + 2 * t + pb]);
             if (t == 1) umma_commit(&bar[kBarKvEmpty + st]);
             if (jj == n - 1) umma_commit(&bar[kBarOFull + t]);
           }
@@ -296,8 +293,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         for (int t = 0; t < 2 && ok; ++t) {
+          // S/P buffer b of tile t was last read by PV of stage g - 2.
           if (g >= 2 &&
-              !wait_or_flag(&bar[kBarSEmpty + 2 * t + b], ((g >> 1) - 1) & 1, status)) {
+              !wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status)) {
             ok = false;
             break;
           }
@@ -330,7 +328,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     const int rows_used = G * TQ;
-    uint8_t* prow = sp + t * S::kP + row * 128;
     uint32_t t_iter = 0, g0 = 0;
     while (true) {
       if (!wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
@@ -354,9 +351,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         float x[kTcKeys];
         tmem_ld64f(lane_base + S::col_s(t, b), x);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarSEmpty + 2 * t + b]);
 
         const int kb = j * kTcKeys;
         const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this row
@@ -373,13 +367,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
                          p.scale_log2;
-        // P_t was last read (and O_t last written) by PV of stage g - 1.
-        if (g >= 1 && !wait_or_flag(&bar[kBarPvDone + t], (g - 1) & 1, status)) {
-          ok = false;
-          break;
-        }
         const bool need = m_ref != -INFINITY && mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
+          // O_t must hold PV of stage g - 1 before it is rescaled.
+          const uint32_t gp = g - 1;
+          if (!wait_or_flag(&bar[kBarPvDone + 2 * t + (gp & 1)], (gp >> 1) & 1, status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const float alpha = need ? ex2(m_ref - mx) : 1.f;
 #pragma unroll 1
@@ -399,24 +394,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (m_ref == -INFINITY) m_ref = mx;
         const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
 
-        // P row (K-major, 128-byte swizzle: 64 keys = one 128-byte row).
+        // P row into tensor memory over its S: column c holds keys 2c, 2c+1.
         float rs8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+        uint32_t w[kTcKeys / 2];
 #pragma unroll
-        for (int c = 0; c < kTcKeys / 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = ex2(fmaf(x[8 * c + 2 * e], p.scale_log2, neg_ref));
-            const float p1 = ex2(fmaf(x[8 * c + 2 * e + 1], p.scale_log2, neg_ref));
-            rs8[2 * e] += p0;
-            rs8[2 * e + 1] += p1;
-            w[e] = pack2<kBF16>(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        for (int c = 0; c < kTcKeys / 2; ++c) {
+          const float p0 = ex2(fmaf(x[2 * c], p.scale_log2, neg_ref));
+          const float p1 = ex2(fmaf(x[2 * c + 1], p.scale_log2, neg_ref));
+          rs8[(2 * c) & 7] += p0;
+          rs8[(2 * c + 1) & 7] += p1;
+          w[c] = pack2<kBF16>(p0, p1);
         }
+        tmem_st32(lane_base + S::col_s(t, b), w);
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
 
         // Keys past the sequence inside the last loaded 16-key box hold
@@ -441,10 +432,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        fence_proxy_async();
+        if (j == n - 1) fence_proxy_async();  // the V rows zeroed above
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarPFull + t]);
+        if (lane == 0) mbar_arrive(&bar[kBarPFull + 2 * t + b]);
       }
       if (!ok) break;
 

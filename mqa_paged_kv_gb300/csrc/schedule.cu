@@ -78,18 +78,19 @@ __device__ __forceinline__ int pf_bucket(int kvlen) {
 // Lanes of the warp that hold the same bucket add their counts together: the
 // group's first lane reserves the group total with one shared-memory atomic,
 // and each lane gets its own start inside that range.  (Hundreds of splits
-// land in the same bucket; one atomic each would serialise them.)
+// land in the same bucket; one atomic each would serialise them.)  Counts are
+// below 128, so a lane's offset inside its group is assembled bit by bit from
+// ballots over the lower lanes of the group.
 __device__ __forceinline__ int warp_aggregated_add(int* counters, int bucket, int count) {
   const int lane = threadIdx.x & 31;
   const unsigned grp = __match_any_sync(0xffffffffu, bucket);
+  const unsigned lower = grp & ((1u << lane) - 1u);
   int before = 0, total = 0;
 #pragma unroll
-  for (int src = 0; src < 32; ++src) {
-    const int c = __shfl_sync(0xffffffffu, count, src);
-    if ((grp >> src) & 1u) {
-      total += c;
-      if (src < lane) before += c;
-    }
+  for (int bit = 0; bit < 7; ++bit) {
+    const unsigned set = __ballot_sync(0xffffffffu, (count >> bit) & 1);
+    before += __popc(set & lower) << bit;
+    total += __popc(set & grp) << bit;
   }
   const int leader = __ffs(grp) - 1;
   int base = 0;
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
 
   // Pass 1: per-sequence plans, split offsets, bucket histograms.
   int carry = 0, tile_total = 0;
+  int first_split_offset = 0;  // this thread's sequence in the first pass
   for (int base = 0; base < p.num_seqs; base += kThreads) {
     const int b = base + tid;
     const SeqPlan s = plan_seq(p, b);
@@ -151,6 +153,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     if (b < p.num_seqs) {
       SeqInfo si;
       si.split_offset = carry + excl;
+      if (base == 0) first_split_offset = si.split_offset;
       si.nsplit = s.nsplit;
       si.tok = s.tok;
       si.qlen = s.qlen;
@@ -200,7 +203,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     const int pos_full = warp_aggregated_add(dec_cnt, dec_bucket(s.chunk_keys), nfull);
     const int pos_tail = warp_aggregated_add(dec_cnt, dec_bucket(tail), s.nsplit > 0 ? 1 : 0);
     if (b >= p.num_seqs) continue;
-    const int split_offset = p.seq_info[b].split_offset;
+    const int split_offset = p.num_seqs <= kThreads ? first_split_offset
+                                                    : p.seq_info[b].split_offset;
     for (int sp = 0; sp < s.nsplit; ++sp) {
       DecPair d;
       d.b = b;
