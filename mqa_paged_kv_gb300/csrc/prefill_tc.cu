@@ -89,6 +89,14 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, uin
   return false;
 }
 
+// Warp-uniform form: every lane polls and the lanes agree on the outcome,
+// so a timeout seen by only some lanes cannot split the warp before the
+// warp-wide (elect.sync) MMA issue.
+__device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity,
+                                                  uint32_t* status) {
+  return __all_sync(0xffffffffu, wait_or_flag(bar, parity, status));
+}
+
 }  // namespace
 
 template <bool kBF16, int D>
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t it = 0;
       if (lane == 0) it = atomicAdd(&p.hdr->prefill_grab, 1u);
       it = __shfl_sync(0xffffffffu, it, 0);
-      if (t_iter > 0 && !wait_or_flag(&bar[kBarQEmpty], (t_iter - 1) & 1, status)) break;
+      if (t_iter > 0 && !warp_wait_or_flag(&bar[kBarQEmpty], (t_iter - 1) & 1, status)) break;
       if (it >= num_items) {
         if (lane == 0) {
           meta->done = 1;
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int kb = 0; kb < nkv; kb += kTcKeys, ++g) {
         const int st = static_cast<int>(g % kTcStages);
         if (g >= kTcStages &&
-            !wait_or_flag(&bar[kBarKvEmpty + st], ((g / kTcStages) - 1) & 1, status)) {
+            !warp_wait_or_flag(&bar[kBarKvEmpty + st], ((g / kTcStages) - 1) & 1, status)) {
           ok = false;
           break;
         }
@@ -243,81 +251,91 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this branch and waits on the barriers together;
+    // elect.sync inside each MMA picks the issuing lane.  Each group of MMAs
+    // is straight-line code on descriptors prepared up front: the tensor
+    // pipe is fed at its full rate only when no branch or runtime trip count
+    // sits between two tcgen05.mma (measured on this part: a
+    // data-independent branch inside the issue loop halves the rate).
+    //
+    // Issue order per step j: QK_0(j), PV_0(j-1), QK_1(j), PV_1(j-1).  The
+    // tiles alternate, so every barrier a group waits on was armed at least
+    // one group earlier: S buffer reuse (QK_t(j) after PV_t(j-2)) has twelve
+    // MMAs of slack, and the softmax of tile t on stage j-1 runs while the
+    // pipe works on the other tile.
     constexpr uint32_t kIdQK = idesc_f16(kTcRows, kTcKeys, kBF16, false, false);
     constexpr uint32_t kIdPV = idesc_f16(kTcRows, D, kBF16, false, true);
-    const uint32_t q_addr = smem_u32(sq);
-    const uint32_t kv_addr = smem_u32(skv);
+    constexpr int kQkSteps = D / 16;
+    // Adding (byte offset >> 4) to a descriptor moves its start address; the
+    // 14-bit field cannot carry because shared-memory offsets stay below
+    // 256 KB.
+    const uint64_t dq = sdesc_sw128(smem_u32(sq), 16, 1024);
+    const uint64_t dk = sdesc_sw128(smem_u32(skv), 16, 1024);
+    const uint64_t dv = sdesc_sw128(smem_u32(skv) + S::kKV, S::kKVRegion, 1024);
     uint32_t t_iter = 0, g0 = 0;
     bool ok = true;
     while (ok) {
-      if (!wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
+      if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
       const TcMeta m = *meta;
+      __syncwarp();
       if (m.done) break;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
       tc_fence_after();
 
-      auto issue_pv = [&](int jj) -> bool {
-        const uint32_t g = g0 + jj;
-        const int st = static_cast<int>(g % kTcStages);
-        const int keys = min(kTcKeys, m.nkv - jj * kTcKeys);
-        const int ksteps = (keys + 15) / 16;
-        const int pb = static_cast<int>(g & 1);
-        for (int t = 0; t < 2; ++t) {
-          if (!wait_or_flag(&bar[kBarPFull + 2 * t + pb], (g >> 1) & 1, status)) return false;
-          if (jj == 0 && t_iter > 0 &&
-              !wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status))
-            return false;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t vbase = kv_addr + st * S::kStage + S::kKV;
-            const uint32_t pcol = tmem + S::col_s(t, pb);
-            for (int ks = 0; ks < ksteps; ++ks) {
-              const uint64_t bd = sdesc_sw128(vbase + ks * 2048, S::kKVRegion, 1024);
-              umma_f16_ts(tmem + S::col_o(t), pcol + ks * 8, bd, kIdPV, (jj > 0 || ks > 0) ? 1u : 0u);
-            }
-            umma_commit(&bar[kBarPvDone + 2 * t + pb]);
-            if (t == 1) umma_commit(&bar[kBarKvEmpty + st]);
-            if (jj == n - 1) umma_commit(&bar[kBarOFull + t]);
-          }
-          __syncwarp();
-        }
-        return true;
-      };
-
-      for (int j = 0; j < n && ok; ++j) {
-        const uint32_t g = g0 + j;
+      for (int j = 0; j <= n && ok; ++j) {
+        const uint32_t g = g0 + j;  // stage of the QK groups
         const int st = static_cast<int>(g % kTcStages);
         const int b = static_cast<int>(g & 1);
-        if (!wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
+        const uint32_t gp = g - 1;  // stage of the PV groups
+        const int stp = static_cast<int>(gp % kTcStages);
+        const int pb = static_cast<int>(gp & 1);
+        if (j < n && !warp_wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
           ok = false;
           break;
         }
-        for (int t = 0; t < 2 && ok; ++t) {
-          // S/P buffer b of tile t was last read by PV of stage g - 2.
-          if (g >= 2 &&
-              !wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t kbase = kv_addr + st * S::kStage;
-            const uint32_t qbase = q_addr + t * S::kQ;
+        const uint64_t dks = dk + static_cast<uint64_t>((st * S::kStage) >> 4);
+        const uint64_t dvs = dv + static_cast<uint64_t>((stp * S::kStage) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              umma_f16(tmem + S::col_s(t, b),
-                       sdesc_sw128(qbase + (ks >> 2) * S::kQRegion + (ks & 3) * 32, 16, 1024),
-                       sdesc_sw128(kbase + (ks >> 2) * S::kKVRegion + (ks & 3) * 32, 16, 1024),
-                       kIdQK, ks > 0 ? 1u : 0u);
+        for (int t = 0; t < 2; ++t) {
+          if (j < n) {
+            // S/P buffer b of tile t was last read by PV of stage g - 2.
+            if (g >= 2 &&
+                !warp_wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status)) {
+              ok = false;
+              break;
             }
-            umma_commit(&bar[kBarSFull + 2 * t + b]);
-            if (t == 1 && j == n - 1) umma_commit(&bar[kBarQEmpty]);
+            tc_fence_after();
+            const uint32_t d = tmem + S::col_s(t, b);
+#pragma unroll
+            for (int ks = 0; ks < kQkSteps; ++ks)
+              umma_f16_warp(d, dq + ((t * S::kQ + (ks >> 2) * S::kQRegion + (ks & 3) * 32) >> 4),
+                            dks + (((ks >> 2) * S::kKVRegion + (ks & 3) * 32) >> 4), kIdQK,
+                            ks > 0 ? 1u : 0u);
+            umma_commit_warp(&bar[kBarSFull + 2 * t + b]);
+            if (t == 1 && j == n - 1) umma_commit_warp(&bar[kBarQEmpty]);
           }
-          __syncwarp();
+          if (j >= 1) {
+            // All four 16-key steps run on every stage: past the sequence P
+            // is 0 and the V rows are zero (zero-filled boxes, or zeroed by
+            // the softmax warps inside the last box).
+            if (!warp_wait_or_flag(&bar[kBarPFull + 2 * t + pb], (gp >> 1) & 1, status) ||
+                (j == 1 && t_iter > 0 &&
+                 !warp_wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + S::col_o(t), a = tmem + S::col_s(t, pb);
+            umma_f16_ts_warp(d, a, dvs, kIdPV, j > 1 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 1; ks < kTcSub; ++ks)
+              umma_f16_ts_warp(d, a + ks * 8, dvs + ((ks * 2048) >> 4), kIdPV, 1u);
+            umma_commit_warp(&bar[kBarPvDone + 2 * t + pb]);
+            if (t == 1) umma_commit_warp(&bar[kBarKvEmpty + stp]);
+            if (j == n) umma_commit_warp(&bar[kBarOFull + t]);
+          }
         }
-        if (ok && j >= 1 && !issue_pv(j - 1)) ok = false;
       }
-      if (!ok || !issue_pv(n - 1)) break;
       g0 += n;
       ++t_iter;
     }
@@ -330,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int rows_used = G * TQ;
     uint32_t t_iter = 0, g0 = 0;
     while (true) {
-      if (!wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
+      if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
       const TcMeta m = *meta;
       __syncwarp();
       if (m.done) break;
@@ -344,7 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int j = 0; j < n; ++j) {
         const uint32_t g = g0 + j;
         const int b = static_cast<int>(g & 1);
-        if (!wait_or_flag(&bar[kBarSFull + 2 * t + b], (g >> 1) & 1, status)) {
+        if (!warp_wait_or_flag(&bar[kBarSFull + 2 * t + b], (g >> 1) & 1, status)) {
           ok = false;
           break;
         }
@@ -371,7 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (__any_sync(0xffffffffu, need)) {
           // O_t must hold PV of stage g - 1 before it is rescaled.
           const uint32_t gp = g - 1;
-          if (!wait_or_flag(&bar[kBarPvDone + 2 * t + (gp & 1)], (gp >> 1) & 1, status)) {
+          if (!warp_wait_or_flag(&bar[kBarPvDone + 2 * t + (gp & 1)], (gp >> 1) & 1, status)) {
             ok = false;
             break;
           }
@@ -418,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int r1 = min(kTcKeys, (r0 + 15) / 16 * 16);
           if (r1 > r0) {
             const int st = static_cast<int>(g % kTcStages);
-            if (!wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
+            if (!warp_wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
               ok = false;
               break;
             }
@@ -441,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!ok) break;
 
       // Epilogue: O_t / l for the valid rows.
-      if (!wait_or_flag(&bar[kBarOFull + t], t_iter & 1, status)) break;
+      if (!warp_wait_or_flag(&bar[kBarOFull + t], t_iter & 1, status)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint16_t* orow = static_cast<uint16_t*>(p.out) +
