@@ -229,6 +229,16 @@ PA_API void pa_profile_next_call(void* start_event, void* stop_event);
 PA_API int pa_version(void);
 PA_API int pa_last_launch_count(void);
 
+/*
+ * The CUDA runtime error (a cudaError_t value) behind the most recent
+ * PA_ERR_CUDA that a launch, function-attribute or stream call on the
+ * calling thread produced, and its text; 0 and "no error" until one has
+ * occurred.  Kept per host thread; a later successful call does not clear
+ * it.  The pages define no such call: it only explains PA_ERR_CUDA.
+ */
+PA_API int pa_last_cuda_error(void);
+PA_API const char* pa_last_cuda_error_string(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,10 @@ _lib.pa_version.argtypes = []
 _lib.pa_version.restype = _I
 _lib.pa_last_launch_count.argtypes = []
 _lib.pa_last_launch_count.restype = _I
+_lib.pa_last_cuda_error.argtypes = []
+_lib.pa_last_cuda_error.restype = _I
+_lib.pa_last_cuda_error_string.argtypes = []
+_lib.pa_last_cuda_error_string.restype = ctypes.c_char_p
 _lib.reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]
 _lib.reshape_and_cache.restype = _I
 _lib.paged_attn_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, _I, _I]
@@ -63,7 +67,8 @@ _lib.paged_attn_decode_noalloc.restype = _I
 _lib.pa_profile_next_call.argtypes = [_P, _P]
 _lib.pa_profile_next_call.restype = None
 
-EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_launch_count", "reshape_and_cache",
+EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_launch_count",
+            "pa_last_cuda_error", "pa_last_cuda_error_string", "reshape_and_cache",
             "paged_attn_workspace_bytes", "paged_attn_decode",
             "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
             "pa_read_device_status", "paged_attn_decode_noalloc"]
@@ -72,7 +77,10 @@ EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_l
 class PagedAttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} ({status})")
+        msg = f"{where}: {status_string(status)} ({status})"
+        if status == -7:  # PA_ERR_CUDA: name the runtime error behind it
+            msg += f": {_lib.pa_last_cuda_error_string().decode()} ({_lib.pa_last_cuda_error()})"
+        super().__init__(msg)
 
 
 def status_string(status: int) -> str:

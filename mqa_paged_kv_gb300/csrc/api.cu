@@ -24,6 +24,16 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
 thread_local int g_last_launches = 0;
+thread_local int g_last_cuda_error = 0;
+
+// Takes the CUDA runtime's pending error (the one behind a failed launch,
+// attribute or synchronize call) for pa_last_cuda_error and returns
+// PA_ERR_CUDA.
+int cuda_error() {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
+}
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 
@@ -169,9 +179,12 @@ int check_workspace(const void* ws, size_t bytes, const WsLayout& L) {
 }
 
 int finish(int launched) {
-  if (launched < 0) return PA_ERR_CUDA;
+  if (launched < 0) return cuda_error();
   g_last_launches = launched;
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return PA_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -198,6 +211,13 @@ const char* pa_status_string(int status) {
 }
 
 int pa_version(void) { return 1; }
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* pa_last_cuda_error_string(void) {
+  return g_last_cuda_error == 0 ? "no error"
+                                : cudaGetErrorString(static_cast<cudaError_t>(g_last_cuda_error));
+}
 
 int pa_last_launch_count(void) { return g_last_launches; }
 
@@ -300,10 +320,10 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
 
   const ProfileScope prof(st);
   int n = 0, r;
-  if ((r = launch_prepare(pp, bf16, st)) < 0) return PA_ERR_CUDA;
+  if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
   n += r;
   prof.begin();
-  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return PA_ERR_CUDA;
+  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return cuda_error();
   n += r;
   prof.end();
   if (num_splits != 1) {
@@ -315,7 +335,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
     cp.num_seqs = num_seqs;
     cp.num_heads = num_heads;
     cp.head_dim = head_dim;
-    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return PA_ERR_CUDA;
+    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
     n += r;
   }
   return finish(n);
@@ -421,16 +441,16 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
 
   const ProfileScope prof(st);
   int n = 0, r;
-  if ((r = launch_prepare(pp, bf16, st)) < 0) return PA_ERR_CUDA;
+  if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
   n += r;
   prof.begin();
   if (max_query_len > 1) {
     if ((r = launch_prefill_tc(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
                                dev.num_sms)) < 0)
-      return PA_ERR_CUDA;
+      return cuda_error();
     n += r;
   }
-  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return PA_ERR_CUDA;
+  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return cuda_error();
   n += r;
   prof.end();
   if (num_splits != 1) {
@@ -442,7 +462,7 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
     cp.num_seqs = num_seqs;
     cp.num_heads = num_heads;
     cp.head_dim = head_dim;
-    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return PA_ERR_CUDA;
+    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
     n += r;
   }
   return finish(n);
@@ -454,14 +474,14 @@ int pa_read_device_status(const void* workspace, int clear, uint32_t* flags, pa_
   const WsHeader* hdr = static_cast<const WsHeader*>(workspace);
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, &hdr->status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return PA_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    return cuda_error();
+  if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_error();
   *flags = v;
   if (clear) {
     if (cudaMemsetAsync(const_cast<uint32_t*>(&hdr->status), 0, sizeof(uint32_t), st) !=
         cudaSuccess)
       return PA_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_error();
   }
   return PA_OK;
 }

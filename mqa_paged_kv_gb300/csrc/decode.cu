@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (p_finished) return;
     const int s = static_cast<int>(p_iter % R);
     if (GS > 1 && p_iter >= static_cast<uint32_t>(R)) {
-      if (!mbar_wait(&empty[s], ((p_iter / R) - 1) & 1)) {
+      if (!mbar_wait_warp(&empty[s], ((p_iter / R) - 1) & 1)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         p_finished = true;
         return;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   uint32_t c_iter = 0;
   while (true) {
     const int s = static_cast<int>(c_iter % R);
-    if (!mbar_wait(&full[s], (c_iter / R) & 1)) {
+    if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
       if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
       break;
     }
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   if (producer) {
     while (c_iter < p_iter) {
       const int s = static_cast<int>(c_iter % R);
-      if (!mbar_wait(&full[s], (c_iter / R) & 1)) break;
+      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) break;
       ++c_iter;
     }
   }

@@ -8,23 +8,27 @@
 // that the G query heads sharing a KV head share its cache reads and do the
 // dot products on tensor cores.  A Q tile packs those G heads times 128 / G
 // consecutive query tokens as the M = 128 rows of the MMA (row r = token * G
-// + head), and each CTA works on two such tiles (A: the first 128 / G
-// tokens, B: the next) of one sequence and KV head, so every 64-key K/V
+// + head), and each CTA works on two such tiles (0: the first 128 / G
+// tokens, 1: the next) of one sequence and KV head, so every 64-key K/V
 // stage gathered from the cache feeds 256 rows.
 //
 // Warp roles (one CTA per SM, persistent over a device tile list):
 //   warp 0     TMA producer: the two Q tiles (one 3-D box per 64 columns
-//              each), then the visible keys in 64-key stages through a
-//              5-deep ring; a stage is 16-key boxes gathered through the
-//              block table, one box per lane, issued by one instruction;
-//   warp 1     MMA issuer (one thread): S_t = Q_t K^T into tensor memory
-//              (two S buffers per tile), O_t += P_t V with P_t read from
-//              tensor memory (O in tensor memory);
-//   warps 2-9  softmax, four warps per tile, one thread per row (= TMEM
+//              each), then K and V of the visible keys in 64-key stages
+//              through one ring of slots, in the order the MMAs consume
+//              them (K0, K1, V0, K2, V1, ...); a slot is 16-key boxes
+//              gathered through the block table, one box per lane, issued
+//              by one instruction;
+//   warps 1-2  MMA issuers, one per tile: S_t = Q_t K^T (M 128, N 64)
+//              into one of two S buffers in tensor memory, O_t += P_t V
+//              with P_t read from tensor memory (O in tensor memory);
+//   warps 3-10 softmax, four warps per tile, one thread per row (= TMEM
 //              lane): scale, bottom-right causal mask, running max,
-//              P = 2^(x*scale - m) in the element type written back over
-//              its own S buffer in tensor memory (so shared memory holds
-//              only Q and the K/V ring), fp32 row sum, and the epilogue O / l.
+//              P = 2^(x*scale - m) in the element type written over the
+//              first half of its own S buffer in tensor memory, fp32 row
+//              sum, and the epilogue O / l.
+// Tensor memory holds two 64-column S buffers per tile and O_0, O_1, so the
+// QK of the next stage runs while the softmax works on the current one.
 // The running max is a reference that only moves when a row max exceeds it
 // by more than 2^8 (then O and l are rescaled in place); between moves P
 // stays below 256, well inside the element type.  Row maxima run over raw
@@ -37,11 +41,11 @@ namespace pa {
 namespace {
 
 constexpr int kTcRows = 128;              // M of one tile
-constexpr int kTcKeys = 64;               // keys per stage
-constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per stage
-constexpr int kTcStages = 5;              // K/V ring depth
+constexpr int kTcKeys = 64;               // keys per stage: N of QK, K of PV
+constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per slot; PV K-steps
 constexpr int kTcSoftmaxWarps = 8;
-constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
+constexpr int kTcFirstSoftmaxWarp = 3;  // warp 0 producer, warps 1-2 MMA issuers
+constexpr int kTcThreads = (kTcFirstSoftmaxWarp + kTcSoftmaxWarps) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 of the largest unnormalised P
 
 struct TcMeta {
@@ -51,37 +55,44 @@ struct TcMeta {
 enum : int {
   kBarQFull = 0,
   kBarQEmpty,
-  kBarKvFull,                              // [stages]
-  kBarKvEmpty = kBarKvFull + kTcStages,    // [stages]
-  kBarSFull = kBarKvEmpty + kTcStages,     // [tile][buffer]
-  kBarPFull = kBarSFull + 4,               // [tile][buffer]
-  kBarPvDone = kBarPFull + 4,              // [tile][buffer]
-  kBarOFull = kBarPvDone + 4,              // [tile]
-  kBarOEmpty = kBarOFull + 2,              // [tile]
-  kNumBars = kBarOEmpty + 2
+  kBarSFull,                  // [tile][buffer]
+  kBarPFull = kBarSFull + 4,  // [tile][buffer]
+  kBarPvDone = kBarPFull + 4, // [tile][buffer]
+  kBarOFull = kBarPvDone + 4, // [tile]
+  kBarOEmpty = kBarOFull + 2, // [tile]
+  kBarSlotFull = kBarOEmpty + 2  // [slot], then [slot] of empties
 };
 
 template <int D>
-struct TcSmem {
-  static constexpr int kBoxes = D / 64;            // 64-column halves
-  static constexpr int kQRegion = 128 * 128;       // 128 rows x 128 B
-  static constexpr int kQ = kBoxes * kQRegion;     // one Q tile
-  static constexpr int kKVRegion = kTcKeys * 128;  // 64 keys x 128 B
-  static constexpr int kKV = kBoxes * kKVRegion;   // 64 keys of K (or V)
-  static constexpr int kStage = 2 * kKV;
-  static constexpr int kOffKV = 2 * kQ;
-  static constexpr int kOffBar = kOffKV + kTcStages * kStage;
+struct TcCfg {
+  static constexpr int kBoxes = D / 64;              // 64-column halves
+  static constexpr int kQRegion = 128 * 128;         // 128 rows x 128 B
+  static constexpr int kQ = kBoxes * kQRegion;       // one Q tile
+  static constexpr int kRegion = kTcKeys * 128;      // 64 keys x 128 B
+  static constexpr int kSlot = kBoxes * kRegion;     // 64 keys of K or of V
+  static constexpr int kSlots = D == 128 ? 10 : 20;  // ring depth
+  static constexpr int kBarSlotEmpty = kBarSlotFull + kSlots;
+  static constexpr int kNumBars = kBarSlotEmpty + kSlots;
+  static constexpr int kOffRing = 2 * kQ;
+  static constexpr int kOffBar = kOffRing + kSlots * kSlot;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
   static constexpr int kBytes = kOffTmem + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // tile t, buffer b: S (fp32, 64 columns) at t*128 + b*64, later P (16-bit
-  // pairs, its first 32 columns); O_t at 256 + t*128
-  static constexpr uint32_t col_s(int t, int b) {
-    return static_cast<uint32_t>(t * 128 + b * 64);
-  }
-  static constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * 128); }
+  // S buffer b of tile t (fp32, 64 columns) at t * 128 + b * 64, later P
+  // (16-bit pairs) over its first 32 columns; O_t at 256 + t * D.
+  static constexpr uint32_t col_s(int t, int b) { return static_cast<uint32_t>(t * 128 + b * 64); }
+  static constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * D); }
 };
+
+// Ring positions, relative to the first load of a work item with n stages:
+// K(0), then K(j), V(j - 1) for j = 1 .. n - 1, then V(n - 1).
+__device__ __forceinline__ uint32_t kpos(int j) {
+  return j == 0 ? 0u : static_cast<uint32_t>(2 * j - 1);
+}
+__device__ __forceinline__ uint32_t vpos(int j, int n) {
+  return static_cast<uint32_t>(j == n - 1 ? 2 * n - 1 : 2 * j + 2);
+}
 
 __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, uint32_t* status) {
   if (mbar_wait(bar, parity)) return true;
@@ -90,8 +101,8 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, uin
 }
 
 // Warp-uniform form: every lane polls and the lanes agree on the outcome,
-// so a timeout seen by only some lanes cannot split the warp before the
-// warp-wide (elect.sync) MMA issue.
+// so a timeout seen by only some lanes cannot split the warp ahead of
+// warp-synchronous instructions (elect.sync issue, tcgen05.ld/st).
 __device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity,
                                                   uint32_t* status) {
   return __all_sync(0xffffffffu, wait_or_flag(bar, parity, status));
@@ -99,29 +110,28 @@ __device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity
 
 }  // namespace
 
+// Eleven warps put three on three of the SM's four register files, which
+// caps a thread at 168 registers; a softmax thread's 128 scores fit in that.
 template <bool kBF16, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ CUtensorMap tmq, const PrefillParams p) {
-  using S = TcSmem<D>;
+  using C = TcCfg<D>;
+  constexpr int kSlots = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sq = smem;
-  uint8_t* skv = smem + S::kOffKV;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  TcMeta* meta = reinterpret_cast<TcMeta*>(smem + S::kOffMeta);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffTmem);
+  uint8_t* ring = smem + C::kOffRing;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  TcMeta* meta = reinterpret_cast<TcMeta*>(smem + C::kOffMeta);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar[kBarQFull], 1);
-    mbar_init(&bar[kBarQEmpty], 1 + kTcSoftmaxWarps);  // MMA commit + meta reads
-    for (int i = 0; i < kTcStages; ++i) {
-      mbar_init(&bar[kBarKvFull + i], 1);
-      mbar_init(&bar[kBarKvEmpty + i], 1);
-    }
+    mbar_init(&bar[kBarQEmpty], 2 + kTcSoftmaxWarps);  // two MMA commits + meta reads
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
       mbar_init(&bar[kBarPFull + i], 4);
@@ -131,9 +141,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bar[kBarOFull + t], 1);
       mbar_init(&bar[kBarOEmpty + t], 4);
     }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&bar[kBarSlotFull + i], 1);
+      mbar_init(&bar[C::kBarSlotEmpty + i], 2);  // one commit per tile's MMA warp
+    }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, S::kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -153,13 +167,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tmq);
     }
     const int oob_row = p.num_blocks * Hkv * bs;  // a box here reads zeros
-    constexpr int nb = kTcSub * S::kBoxes;        // K boxes per stage (= V boxes)
-    static_assert(2 * nb <= 32, "one box per lane");
-    const bool is_v = lane >= nb;
-    const int box = is_v ? lane - nb : lane;
-    const int my_j = box / S::kBoxes, my_bx = box % S::kBoxes;
-    uint32_t t_iter = 0, g = 0;
+    constexpr int nb = kTcSub * C::kBoxes;        // boxes per slot
+    static_assert(nb <= 32, "one box per lane");
+    const bool boxer = lane < nb;
+    const int my_j = lane / C::kBoxes, my_bx = lane % C::kBoxes;
+    uint32_t t_iter = 0, c = 0;  // c: ring position of the next load
     bool ok = true;
+
+    // One slot: K or V of one stage, each lane its own 16-key box.
+    auto load_slot = [&](const CUtensorMap* map, int row) -> bool {
+      const int s = static_cast<int>(c % kSlots);
+      if (c >= static_cast<uint32_t>(kSlots) &&
+          !warp_wait_or_flag(&bar[C::kBarSlotEmpty + s], ((c / kSlots) - 1) & 1, status))
+        return false;
+      if (lane == 0) mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
+      __syncwarp();
+      if (boxer)
+        tma_load_2d(ring + s * C::kSlot + my_bx * C::kRegion + my_j * 2048, map, my_bx * 64, row,
+                    &bar[kBarSlotFull + s]);
+      ++c;
+      return true;
+    };
+
     while (ok) {
       uint32_t it = 0;
       if (lane == 0) it = atomicAdd(&p.hdr->prefill_grab, 1u);
@@ -188,12 +217,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m.pad = 0;
         *meta = m;
         mbar_arrive_expect_tx(&bar[kBarQFull],
-                              static_cast<uint32_t>(2 * S::kBoxes * 128 * G * TQ));
+                              static_cast<uint32_t>(2 * C::kBoxes * 128 * G * TQ));
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int bx = 0; bx < S::kBoxes; ++bx)
-            tma_load_3d(sq + t * S::kQ + bx * S::kQRegion, &tmq, bx * 64, kvh * G,
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_3d(sq + t * C::kQ + bx * C::kQRegion, &tmq, bx * 64, kvh * G,
                         tile.tok0 + t * TQ, &bar[kBarQFull]);
       }
       ++t_iter;
@@ -210,13 +239,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int ids = load_window(0);
       int ids_next = load_window(32);
       int lblk = 0, off = 0;  // block and slot of the next 16-key box
-      for (int kb = 0; kb < nkv; kb += kTcKeys, ++g) {
-        const int st = static_cast<int>(g % kTcStages);
-        if (g >= kTcStages &&
-            !warp_wait_or_flag(&bar[kBarKvEmpty + st], ((g / kTcStages) - 1) & 1, status)) {
-          ok = false;
-          break;
-        }
+      // This lane's cache row for stage kb (keys kb .. kb + 127).
+      auto stage_row = [&](int kb) -> int {
         int my_row = oob_row;
 #pragma unroll
         for (int j = 0; j < kTcSub; ++j) {
@@ -239,41 +263,104 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++lblk;
           }
         }
-        if (lane == 0)
-          mbar_arrive_expect_tx(&bar[kBarKvFull + st], static_cast<uint32_t>(S::kStage));
-        __syncwarp();
-        if (lane < 2 * nb) {
-          uint8_t* dst = skv + st * S::kStage + (is_v ? S::kKV : 0) + my_bx * S::kKVRegion +
-                         my_j * 2048;
-          tma_load_2d(dst, is_v ? &tmv : &tmk, my_bx * 64, my_row, &bar[kBarKvFull + st]);
-        }
+        return my_row;
+      };
+
+      // K(0), then K(j), V(j - 1) for j = 1 .. n - 1, then V(n - 1): the
+      // order the MMAs consume them in.
+      const int n = (nkv + kTcKeys - 1) / kTcKeys;
+      int prev_row = oob_row;
+      for (int j = 0; j < n && ok; ++j) {
+        const int row = stage_row(j * kTcKeys);
+        ok = load_slot(&tmk, row);
+        if (ok && j >= 1) ok = load_slot(&tmv, prev_row);
+        prev_row = row;
       }
+      if (ok) ok = load_slot(&tmv, prev_row);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this branch and waits on the barriers together;
-    // elect.sync inside each MMA picks the issuing lane.  Each group of MMAs
-    // is straight-line code on descriptors prepared up front: the tensor
-    // pipe is fed at its full rate only when no branch or runtime trip count
-    // sits between two tcgen05.mma (measured on this part: a
-    // data-independent branch inside the issue loop halves the rate).
-    //
-    // Issue order per step j: QK_0(j), PV_0(j-1), QK_1(j), PV_1(j-1).  The
-    // tiles alternate, so every barrier a group waits on was armed at least
-    // one group earlier: S buffer reuse (QK_t(j) after PV_t(j-2)) has twelve
-    // MMAs of slack, and the softmax of tile t on stage j-1 runs while the
-    // pipe works on the other tile.
+    // Leave no copy in flight (the consumers may have stopped early on a
+    // timeout): wait, bounded, for the newest load of every slot.
+    for (uint32_t q = c > static_cast<uint32_t>(kSlots) ? c - kSlots : 0u; q < c; ++q)
+      if (!warp_wait_or_flag(&bar[kBarSlotFull + q % kSlots], (q / kSlots) & 1, status)) break;
+  } else if (warp < kTcFirstSoftmaxWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // One warp per Q tile, so each tile's chain advances on its own while
+    // the pipe runs the other tile's groups.  Per tile the QK of stage j + 1
+    // is issued before the PV of stage j, so it runs while the softmax works
+    // on stage j.  The warp waits on the barriers together and elect.sync
+    // inside each MMA picks the issuing lane.  Each group of MMAs is
+    // straight-line code on descriptors prepared up front: the tensor pipe
+    // is fed at its full rate only when no branch or runtime trip count sits
+    // between two tcgen05.mma (measured on this part: a data-independent
+    // branch inside the issue loop halves the rate).  P lives in the S
+    // buffer that the QK two stages later overwrites, and MMAs on different
+    // accumulators are not ordered, so that QK waits for the PV to complete.
+    const int t = warp - 1;
     constexpr uint32_t kIdQK = idesc_f16(kTcRows, kTcKeys, kBF16, false, false);
     constexpr uint32_t kIdPV = idesc_f16(kTcRows, D, kBF16, false, true);
     constexpr int kQkSteps = D / 16;
     // Adding (byte offset >> 4) to a descriptor moves its start address; the
     // 14-bit field cannot carry because shared-memory offsets stay below
     // 256 KB.
-    const uint64_t dq = sdesc_sw128(smem_u32(sq), 16, 1024);
-    const uint64_t dk = sdesc_sw128(smem_u32(skv), 16, 1024);
-    const uint64_t dv = sdesc_sw128(smem_u32(skv) + S::kKV, S::kKVRegion, 1024);
-    uint32_t t_iter = 0, g0 = 0;
+    const uint64_t dq = sdesc_sw128(smem_u32(sq + t * C::kQ), 16, 1024);
+    const uint64_t dk = sdesc_sw128(smem_u32(ring), 16, 1024);             // K-major
+    const uint64_t dv = sdesc_sw128(smem_u32(ring), C::kRegion, 1024);     // MN-major
+    const uint32_t dout = tmem + C::col_o(t);
+    uint32_t t_iter = 0, g0 = 0, c0 = 0;
     bool ok = true;
+
+    // S_t(j) = Q_t K(j)^T once K(j) landed and the PV two stages back no
+    // longer reads that S buffer.
+    auto issue_qk = [&](int j, int n) -> bool {
+      const uint32_t g = g0 + j;
+      const int b = static_cast<int>(g & 1);
+      const uint32_t ck = c0 + kpos(j);
+      const int sk = static_cast<int>(ck % kSlots);
+      if (!warp_wait_or_flag(&bar[kBarSlotFull + sk], (ck / kSlots) & 1, status) ||
+          (g >= 2 &&
+           !warp_wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status)))
+        return false;
+      tc_fence_after();
+      const uint64_t dks = dk + static_cast<uint64_t>((sk * C::kSlot) >> 4);
+      const uint32_t ds = tmem + C::col_s(t, b);
+#pragma unroll
+      for (int ks = 0; ks < kQkSteps; ++ks)
+        umma_f16_warp(ds, dq + (((ks >> 2) * C::kQRegion + (ks & 3) * 32) >> 4),
+                      dks + (((ks >> 2) * C::kRegion + (ks & 3) * 32) >> 4), kIdQK,
+                      ks > 0 ? 1u : 0u);
+      umma_commit_warp(&bar[kBarSFull + 2 * t + b]);
+      umma_commit_warp(&bar[C::kBarSlotEmpty + sk]);
+      if (j == n - 1) umma_commit_warp(&bar[kBarQEmpty]);
+      return true;
+    };
+    // O_t += P_t(j) V(j) once V(j) landed, P_t(j) is written and (first
+    // stage) the previous item's epilogue has read O_t.  All four 16-key
+    // steps run on every stage: past the sequence P is 0 and the V rows are
+    // zero (zero-filled boxes, or zeroed by the softmax warps inside the
+    // last box).
+    auto issue_pv = [&](int j, int n) -> bool {
+      const uint32_t g = g0 + j;
+      const int b = static_cast<int>(g & 1);
+      const uint32_t cv = c0 + vpos(j, n);
+      const int sv = static_cast<int>(cv % kSlots);
+      if (!warp_wait_or_flag(&bar[kBarSlotFull + sv], (cv / kSlots) & 1, status) ||
+          !warp_wait_or_flag(&bar[kBarPFull + 2 * t + b], (g >> 1) & 1, status) ||
+          (j == 0 && t_iter > 0 &&
+           !warp_wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status)))
+        return false;
+      tc_fence_after();
+      const uint64_t dvs = dv + static_cast<uint64_t>((sv * C::kSlot) >> 4);
+      const uint32_t ap = tmem + C::col_s(t, b);
+      umma_f16_ts_warp(dout, ap, dvs, kIdPV, j > 0 ? 1u : 0u);
+#pragma unroll
+      for (int ks = 1; ks < kTcSub; ++ks)
+        umma_f16_ts_warp(dout, ap + ks * 8, dvs + ((ks * 2048) >> 4), kIdPV, 1u);
+      umma_commit_warp(&bar[kBarPvDone + 2 * t + b]);
+      umma_commit_warp(&bar[C::kBarSlotEmpty + sv]);
+      if (j == n - 1) umma_commit_warp(&bar[kBarOFull + t]);
+      return true;
+    };
+
     while (ok) {
       if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
       const TcMeta m = *meta;
@@ -281,72 +368,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (m.done) break;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
       tc_fence_after();
-
-      for (int j = 0; j <= n && ok; ++j) {
-        const uint32_t g = g0 + j;  // stage of the QK groups
-        const int st = static_cast<int>(g % kTcStages);
-        const int b = static_cast<int>(g & 1);
-        const uint32_t gp = g - 1;  // stage of the PV groups
-        const int stp = static_cast<int>(gp % kTcStages);
-        const int pb = static_cast<int>(gp & 1);
-        if (j < n && !warp_wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
-          ok = false;
-          break;
-        }
-        const uint64_t dks = dk + static_cast<uint64_t>((st * S::kStage) >> 4);
-        const uint64_t dvs = dv + static_cast<uint64_t>((stp * S::kStage) >> 4);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j < n) {
-            // S/P buffer b of tile t was last read by PV of stage g - 2.
-            if (g >= 2 &&
-                !warp_wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + S::col_s(t, b);
-#pragma unroll
-            for (int ks = 0; ks < kQkSteps; ++ks)
-              umma_f16_warp(d, dq + ((t * S::kQ + (ks >> 2) * S::kQRegion + (ks & 3) * 32) >> 4),
-                            dks + (((ks >> 2) * S::kKVRegion + (ks & 3) * 32) >> 4), kIdQK,
-                            ks > 0 ? 1u : 0u);
-            umma_commit_warp(&bar[kBarSFull + 2 * t + b]);
-            if (t == 1 && j == n - 1) umma_commit_warp(&bar[kBarQEmpty]);
-          }
-          if (j >= 1) {
-            // All four 16-key steps run on every stage: past the sequence P
-            // is 0 and the V rows are zero (zero-filled boxes, or zeroed by
-            // the softmax warps inside the last box).
-            if (!warp_wait_or_flag(&bar[kBarPFull + 2 * t + pb], (gp >> 1) & 1, status) ||
-                (j == 1 && t_iter > 0 &&
-                 !warp_wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + S::col_o(t), a = tmem + S::col_s(t, pb);
-            umma_f16_ts_warp(d, a, dvs, kIdPV, j > 1 ? 1u : 0u);
-#pragma unroll
-            for (int ks = 1; ks < kTcSub; ++ks)
-              umma_f16_ts_warp(d, a + ks * 8, dvs + ((ks * 2048) >> 4), kIdPV, 1u);
-            umma_commit_warp(&bar[kBarPvDone + 2 * t + pb]);
-            if (t == 1) umma_commit_warp(&bar[kBarKvEmpty + stp]);
-            if (j == n) umma_commit_warp(&bar[kBarOFull + t]);
-          }
-        }
+      ok = issue_qk(0, n);
+      for (int j = 0; j < n && ok; ++j) {
+        if (j + 1 < n) ok = issue_qk(j + 1, n);
+        if (ok) ok = issue_pv(j, n);
       }
       g0 += n;
+      c0 += 2 * n;
       ++t_iter;
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) / 4;    // Q tile of this warp
+    const int t = (warp - kTcFirstSoftmaxWarp) / 4;  // Q tile of this warp
     const int quarter = warp & 3;    // TMEM lanes 32*quarter ..
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     const int rows_used = G * TQ;
-    uint32_t t_iter = 0, g0 = 0;
+    uint32_t t_iter = 0, g0 = 0, c0 = 0;
     while (true) {
       if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
       const TcMeta m = *meta;
@@ -368,7 +406,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         float x[kTcKeys];
-        tmem_ld64f(lane_base + S::col_s(t, b), x);
+        tmem_ld64f(lane_base + C::col_s(t, b), x);
 
         const int kb = j * kTcKeys;
         const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this row
@@ -388,8 +426,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool need = m_ref != -INFINITY && mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           // O_t must hold PV of stage g - 1 before it is rescaled.
-          const uint32_t gp = g - 1;
-          if (!warp_wait_or_flag(&bar[kBarPvDone + 2 * t + (gp & 1)], (gp >> 1) & 1, status)) {
+          if (g >= 1 && !warp_wait_or_flag(&bar[kBarPvDone + 2 * t + ((g - 1) & 1)],
+                                           ((g - 1) >> 1) & 1, status)) {
             ok = false;
             break;
           }
@@ -398,12 +436,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
             uint32_t r[16];
-            tmem_ld16(lane_base + S::col_o(t) + c * 16, r);
+            tmem_ld16(lane_base + C::col_o(t) + c * 16, r);
 #pragma unroll
             for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st16(lane_base + S::col_o(t) + c * 16, r);
+            tmem_st16(lane_base + C::col_o(t) + c * 16, r);
           }
-          tmem_wait_st();
           if (need) {
             l *= alpha;
             m_ref = mx;
@@ -412,45 +449,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (m_ref == -INFINITY) m_ref = mx;
         const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
 
-        // P row into tensor memory over its S: column c holds keys 2c, 2c+1.
+        // P = 2^(x * scale - m_ref), in place, then its row sum, then the P
+        // row into tensor memory over the first half of its S: column c
+        // holds keys 2c, 2c+1 (those S values are already in registers).
+#pragma unroll
+        for (int i = 0; i < kTcKeys; ++i) x[i] = ex2(fmaf(x[i], p.scale_log2, neg_ref));
         float rs8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
-        uint32_t w[kTcKeys / 2];
+        for (int e = 0; e < 8; ++e) rs8[e] = x[e];
 #pragma unroll
-        for (int c = 0; c < kTcKeys / 2; ++c) {
-          const float p0 = ex2(fmaf(x[2 * c], p.scale_log2, neg_ref));
-          const float p1 = ex2(fmaf(x[2 * c + 1], p.scale_log2, neg_ref));
-          rs8[(2 * c) & 7] += p0;
-          rs8[(2 * c + 1) & 7] += p1;
-          w[c] = pack2<kBF16>(p0, p1);
-        }
-        tmem_st32(lane_base + S::col_s(t, b), w);
+        for (int i = 8; i < kTcKeys; ++i) rs8[i & 7] += x[i];
         l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+#pragma unroll
+        for (int h = 0; h < kTcKeys / 32; ++h) {
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) w[c] = pack2<kBF16>(x[32 * h + 2 * c], x[32 * h + 2 * c + 1]);
+          tmem_st16(lane_base + C::col_s(t, b) + 16 * h, w);
+        }
 
         // Keys past the sequence inside the last loaded 16-key box hold
         // whatever the cache slots hold: zero those V rows (P is 0 there,
-        // but 0 * NaN is not).  Both tiles' warps write the same zeros.
+        // but 0 * NaN is not).  Each tile's PV waits only for its own
+        // softmax warps, so both tiles' warps write the same zeros.
         if (j == n - 1) {
           const int r0 = m.nkv - kb;
           const int r1 = min(kTcKeys, (r0 + 15) / 16 * 16);
           if (r1 > r0) {
-            const int st = static_cast<int>(g % kTcStages);
-            if (!warp_wait_or_flag(&bar[kBarKvFull + st], (g / kTcStages) & 1, status)) {
+            const uint32_t cv = c0 + vpos(j, n);
+            const int sv = static_cast<int>(cv % kSlots);
+            if (!warp_wait_or_flag(&bar[kBarSlotFull + sv], (cv / kSlots) & 1, status)) {
               ok = false;
               break;
             }
-            uint8_t* vst = skv + st * S::kStage + S::kKV;
-            const int per_row = S::kBoxes * 8;  // 16-byte chunks per key row
+            uint8_t* vst = ring + sv * C::kSlot;
+            const int per_row = C::kBoxes * 8;  // 16-byte chunks per key row
             const int total = (r1 - r0) * per_row;
             for (int i = row; i < total; i += 128) {
-              const int kr = r0 + i / per_row, c = i % per_row;
-              *reinterpret_cast<uint4*>(vst + (c >> 3) * S::kKVRegion + kr * 128 + (c & 7) * 16) =
+              const int kr = r0 + i / per_row, cc = i % per_row;
+              *reinterpret_cast<uint4*>(vst + (cc >> 3) * C::kRegion + kr * 128 + (cc & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
+            fence_proxy_async();
           }
         }
-        if (j == n - 1) fence_proxy_async();  // the V rows zeroed above
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -468,7 +510,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_base + S::col_o(t) + c * 32, r);
+        tmem_ld32(lane_base + C::col_o(t) + c * 32, r);
         if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -489,6 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarOEmpty + t]);
       g0 += n;
+      c0 += 2 * n;
       ++t_iter;
     }
   }
@@ -496,7 +539,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, S::kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 namespace {
@@ -505,14 +548,14 @@ template <bool kBF16, int D>
 int launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                         const PrefillParams& p, int64_t max_items, cudaStream_t stream,
                         int num_sms) {
-  using S = TcSmem<D>;
-  static_assert(S::kBytes <= 227 * 1024, "one CTA per SM");
+  using C = TcCfg<D>;
+  static_assert(C::kBytes <= 227 * 1024, "one CTA per SM");
   auto kern = prefill_tc_kernel<kBF16, D>;
   static int configured = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured != dev) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) !=
         cudaSuccess)
       return -1;
     configured = dev;
@@ -523,7 +566,7 @@ int launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const CU
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = S::kBytes;
+  cfg.dynamicSmemBytes = C::kBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

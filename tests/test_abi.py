@@ -114,3 +114,9 @@ def test_reshape_and_cache_rejects_bad_arguments(lib):
     assert f(*a) == -8
     a = list(base); a[5] = 0
     assert f(*a) == 0
+
+
+def test_last_cuda_error_starts_clear(lib):
+    # Host-side validation failures are not CUDA errors and leave it clear.
+    assert lib._lib.pa_last_cuda_error() == 0
+    assert lib._lib.pa_last_cuda_error_string() == b"no error"
