@@ -42,6 +42,7 @@ import workloads as W  # noqa: E402
 METRIC = "paged GQA decode KV-cache GB/s (% of GB300 HBM peak); mixed-batch tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse_args():
@@ -74,6 +75,28 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", str(rank)))
     return rank, world, local
+
+
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s) measured for a kernel timed on its own."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s"
+
+
+def prefill_flops(case) -> float:
+    """QK^T and PV of the query chunks (qlen > 1): 4 * Hq * D per visible key."""
+    ql = np.asarray(case.query_lens, dtype=np.int64)
+    cl = np.asarray(case.context_lens, dtype=np.int64)
+    total = 0.0
+    for q, c in zip(ql, cl):
+        if q > 1:  # token i of the chunk sees c - q + i + 1 keys
+            total += 4.0 * case.num_heads * case.head_dim * float(q * (c - q) + q * (q + 1) // 2)
+    return total
 
 
 def measured_hbm_peak():
@@ -143,9 +166,11 @@ class ClockSampler:
 
 
 def kernel_source_sha(fname: str) -> str:
+    """Hash of a kernel's source file and the headers every kernel includes."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "mqa_paged_kv_gb300", "csrc", fname), "rb") as f:
-        h.update(f.read())
+    for part in (fname, "pa_common.cuh", "pa_kernels.cuh"):
+        with open(os.path.join(ROOT, "mqa_paged_kv_gb300", "csrc", part), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -371,6 +396,26 @@ def time_steps(step, steps, warmup, flush, e2e=False):
     return t, kt, h2d, d2h
 
 
+def prefill_roofline(workload: str, seed: int, device, args, flush):
+    """Tensor roofline of prefill_tc_kernel on the query chunks of a mixed
+    batch: the chunks alone (same lengths, seed and shapes, no decode rows)
+    are timed through the same call, so the kernel hook brackets only the
+    prefill kernel (and an empty decode launch)."""
+    pcase = W.mixed_prefill_decode(seed, n_decode=0)
+    pstep = Step(pcase, device, args.splits)
+    _, pkt, _, _ = time_steps(pstep, max(5, args.steps // 2), 3, flush)
+    del pstep
+    flops = prefill_flops(pcase)
+    kern_s = float(pkt.mean()) / 1e3
+    peak, src = measured_bf16_peak()
+    achieved = flops / kern_s / 1e12
+    return {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
+            "peak": peak, "peak_source": src, "unit": "TFLOP/s", "frac": achieved / peak,
+            "kernel_ms": kern_s * 1e3, "algorithmic_flops": flops,
+            "traffic": ncu_traffic("prefill_tc_kernel", "prefill_tc.cu", workload),
+            "timed_on": f"the {pcase.num_seqs} query chunks of {workload} (seed {seed}) alone"}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -418,9 +463,14 @@ def run_ours(args):
     value = kvb * world / step_s / 1e9
     peak, peak_src = measured_hbm_peak()
     achieved = kvb / kern_s / 1e9
-    main_kernel = "decode_kernel" if case.is_decode else "prefill_kernel+decode_kernel"
-    traffic = ncu_traffic("decode_kernel" if case.is_decode else "prefill_kernel",
-                          "decode.cu" if case.is_decode else "prefill.cu", case.name)
+    if case.is_decode:
+        traffic = ncu_traffic("decode_kernel", "decode.cu", case.name)
+        roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
+                    "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                    "frac": achieved / peak, "kernel_ms": kern_s * 1e3,
+                    "algorithmic_bytes": kvb, "traffic": traffic}
+    else:
+        roofline = prefill_roofline(args.workload, args.seed + rank, device, args, flush)
 
     line = {
         "metric": METRIC, "value": value, "unit": units, "n_gpus": world,
@@ -434,10 +484,7 @@ def run_ours(args):
                        step_time_stats=step_stats),
         "hbm_peak_frac": value / world / peak,
         "tokens_per_s": case.total_query_tokens * world / step_s,
-        "roofline": {"bound": "hbm", "kernel": main_kernel, "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": kvb,
-                     "traffic": traffic},
+        "roofline": roofline,
         "e2e": {"value": kvb * world / e2e_s / 1e9, "unit": units, "ms_per_step": e2e_s * 1e3,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
@@ -450,11 +497,13 @@ def run_ours(args):
         mstep = Step(mcase, device, args.splits)
         mt, mkt, _, _ = time_steps(mstep, max(5, args.steps // 2), 3, flush)
         ms = float(mt.mean()) / 1e3
+        del mstep
         line["secondary"] = {"mixed_prefill_decode": {
             "tokens_per_s": mcase.total_query_tokens / ms, "ms_per_step": ms * 1e3,
             "attention_kernels_ms": float(mkt.mean()),
-            "kv_gbs": mcase.kv_bytes() / ms / 1e9, "query_tokens": mcase.total_query_tokens}}
-        del mstep
+            "kv_gbs": mcase.kv_bytes() / ms / 1e9, "query_tokens": mcase.total_query_tokens,
+            "roofline": prefill_roofline("mixed_prefill_decode", args.seed + rank, device,
+                                         args, flush)}}
 
     if rank == 0 and not args.no_cpu_baseline:
         try:
