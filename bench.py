@@ -59,13 +59,20 @@ def parse_args():
                     help="skip the mixed-batch line item")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="cache block size for llama8b_decode / mixed_prefill_decode "
+                         "(the block-size sweep); 16 is the headline configuration")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
 
-def make_workload(name: str, seed: int):
+def make_workload(name: str, seed: int, block_size: int = 16):
     if name.startswith("head_sweep_kv"):
         return W.head_sweep(seed, num_kv_heads=int(name[len("head_sweep_kv"):]))
+    if block_size != 16:
+        if name not in ("llama8b_decode", "mixed_prefill_decode"):
+            raise SystemExit("--block-size applies to llama8b_decode and mixed_prefill_decode")
+        return W.CONFIGS[name](seed, block_size=block_size)
     return W.CONFIGS[name](seed)
 
 
@@ -260,7 +267,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    case = make_workload(args.workload, args.seed)
+    case = make_workload(args.workload, args.seed, args.block_size)
     threads = os.cpu_count() or 1
     rows, kc, vc = oracle_sample_rows(case, 2.0, threads)
     kvb = sample_kv_bytes(case, rows)
@@ -401,7 +408,7 @@ def prefill_roofline(workload: str, seed: int, device, args, flush):
     batch: the chunks alone (same lengths, seed and shapes, no decode rows)
     are timed through the same call, so the kernel hook brackets only the
     prefill kernel (and an empty decode launch)."""
-    pcase = W.mixed_prefill_decode(seed, n_decode=0)
+    pcase = W.mixed_prefill_decode(seed, n_decode=0, block_size=args.block_size)
     pstep = Step(pcase, device, args.splits)
     _, pkt, _, _ = time_steps(pstep, max(5, args.steps // 2), 3, flush)
     del pstep
@@ -427,7 +434,7 @@ def run_ours(args):
     torch.cuda.set_device(device)
     import mqa_paged_kv_gb300  # noqa: F401  (fails loudly when the library is missing)
 
-    case = make_workload(args.workload, args.seed + rank)
+    case = make_workload(args.workload, args.seed + rank, args.block_size)
     step = Step(case, device, args.splits)
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -493,7 +500,7 @@ def run_ours(args):
     }
 
     if not args.no_secondary and args.workload == "llama8b_decode":
-        mcase = W.mixed_prefill_decode(args.seed + rank)
+        mcase = W.mixed_prefill_decode(args.seed + rank, block_size=args.block_size)
         mstep = Step(mcase, device, args.splits)
         mt, mkt, _, _ = time_steps(mstep, max(5, args.steps // 2), 3, flush)
         ms = float(mt.mean()) / 1e3

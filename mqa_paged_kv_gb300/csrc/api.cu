@@ -94,13 +94,14 @@ int current_device(DeviceInfo& info) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D map over a cache [NB * Hkv * bs rows][D]: 16-key x 64-column boxes.
-int encode_cache_map(CUtensorMap* map, const void* base, int64_t rows, int head_dim) {
+// 2-D map over a cache [NB * Hkv * bs rows][D]: box_rows-key x 64-column boxes.
+int encode_cache_map(CUtensorMap* map, const void* base, int64_t rows, int head_dim,
+                     int box_rows = kKeyTile) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kKeyTile)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -384,6 +385,15 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
       PA_OK)
     return rc;
+  // The prefill kernel gathers K/V in boxes of gcd(block_size, 64) keys: a
+  // 64-key stage then takes 64 / box_rows boxes per 64 columns, and larger
+  // blocks mean fewer, larger TMA copies.
+  const int box_rows = (block_size % 64 == 0) ? 64 : (block_size % 32 == 0) ? 32 : 16;
+  CUtensorMap tmk_pf = tmk, tmv_pf = tmv;
+  if (box_rows != kKeyTile && max_query_len > 1) {
+    if ((rc = encode_cache_map(&tmk_pf, k_cache, rows, head_dim, box_rows)) != PA_OK) return rc;
+    if ((rc = encode_cache_map(&tmv_pf, v_cache, rows, head_dim, box_rows)) != PA_OK) return rc;
+  }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const bool bf16 = dtype == PA_BF16;
@@ -420,6 +430,7 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   fp.block_size = block_size;
   fp.num_blocks = num_blocks;
   fp.tokens_per_tile = TQ;
+  fp.box_rows = box_rows;
   fp.scale_log2 = scale * 1.4426950408889634f;
 
   DecodeParams dp;
@@ -445,7 +456,7 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
   n += r;
   prof.begin();
   if (max_query_len > 1) {
-    if ((r = launch_prefill_tc(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
+    if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
                                dev.num_sms)) < 0)
       return cuda_error();
     n += r;

@@ -146,6 +146,7 @@ struct PrefillParams {
   const PfTile* tiles;
   WsHeader* hdr;
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks, tokens_per_tile;
+  int box_rows;  // keys per K/V box: gcd(block_size, 64), so a box never crosses a block
   float scale_log2;
 };
 

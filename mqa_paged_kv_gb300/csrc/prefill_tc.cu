@@ -16,9 +16,9 @@
 //   warp 0     TMA producer: the two Q tiles (one 3-D box per 64 columns
 //              each), then K and V of the visible keys in 64-key stages
 //              through one ring of slots, in the order the MMAs consume
-//              them (K0, K1, V0, K2, V1, ...); a slot is 16-key boxes
-//              gathered through the block table, one box per lane, issued
-//              by one instruction;
+//              them (K0, K1, V0, K2, V1, ...); a slot is boxes of
+//              gcd(block_size, 64) keys gathered through the block table,
+//              one box per lane, issued by one instruction;
 //   warps 1-2  MMA issuers, one per tile: S_t = Q_t K^T (M 128, N 64)
 //              into one of two S buffers in tensor memory, O_t += P_t V
 //              with P_t read from tensor memory (O in tensor memory);
@@ -167,8 +167,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tmq);
     }
     const int oob_row = p.num_blocks * Hkv * bs;  // a box here reads zeros
-    constexpr int nb = kTcSub * C::kBoxes;        // boxes per slot
-    static_assert(nb <= 32, "one box per lane");
+    // A slot is 64 / box_rows boxes of box_rows keys per 64 columns; box j
+    // of column half bx belongs to lane j * kBoxes + bx.
+    const int box_rows = p.box_rows;               // 16, 32 or 64
+    const int kboxes = kTcKeys / box_rows;         // boxes per 64 columns
+    const int nb = kboxes * C::kBoxes;             // boxes per slot (<= 8)
     const bool boxer = lane < nb;
     const int my_j = lane / C::kBoxes, my_bx = lane % C::kBoxes;
     uint32_t t_iter = 0, c = 0;  // c: ring position of the next load
@@ -183,7 +186,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
       __syncwarp();
       if (boxer)
-        tma_load_2d(ring + s * C::kSlot + my_bx * C::kRegion + my_j * 2048, map, my_bx * 64, row,
+        tma_load_2d(ring + s * C::kSlot + my_bx * C::kRegion + my_j * box_rows * 128, map,
+                    my_bx * 64, row,
                     &bar[kBarSlotFull + s]);
       ++c;
       return true;
@@ -238,13 +242,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int ids_base = 0;
       int ids = load_window(0);
       int ids_next = load_window(32);
-      int lblk = 0, off = 0;  // block and slot of the next 16-key box
-      // This lane's cache row for stage kb (keys kb .. kb + 127).
+      int lblk = 0, off = 0;  // block and slot of the next box
+      // This lane's cache row for the stage of keys kb .. kb + 63.
       auto stage_row = [&](int kb) -> int {
         int my_row = oob_row;
 #pragma unroll
         for (int j = 0; j < kTcSub; ++j) {
-          const int key = kb + 16 * j;
+          if (j >= kboxes) break;
+          const int key = kb + box_rows * j;
           if (key < nkv && lblk - ids_base >= 32) {  // windows advance in order
             ids_base += 32;
             ids = ids_next;
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           const int row = (key < nkv && blk >= 0) ? (blk * Hkv + kvh) * bs + off : oob_row;
           if (j == my_j) my_row = row;
-          off += 16;
+          off += box_rows;
           if (off == bs) {
             off = 0;
             ++lblk;
@@ -468,13 +473,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_st16(lane_base + C::col_s(t, b) + 16 * h, w);
         }
 
-        // Keys past the sequence inside the last loaded 16-key box hold
+        // Keys past the sequence inside the last loaded box hold
         // whatever the cache slots hold: zero those V rows (P is 0 there,
         // but 0 * NaN is not).  Each tile's PV waits only for its own
         // softmax warps, so both tiles' warps write the same zeros.
         if (j == n - 1) {
           const int r0 = m.nkv - kb;
-          const int r1 = min(kTcKeys, (r0 + 15) / 16 * 16);
+          const int r1 = min(kTcKeys, (r0 + p.box_rows - 1) / p.box_rows * p.box_rows);
           if (r1 > r0) {
             const uint32_t cv = c0 + vpos(j, n);
             const int sv = static_cast<int>(cv % kSlots);

@@ -101,7 +101,7 @@ def test_group_sizes_decode_and_prefill(G):
     run_and_check(d)
 
 
-@pytest.mark.parametrize("bs", [32, 64, 128, 256])
+@pytest.mark.parametrize("bs", [32, 48, 64, 96, 128, 256])
 def test_block_sizes(bs):
     rng = np.random.default_rng(bs)
     ctx = rng.integers(1, 1200, size=6)

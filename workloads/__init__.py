@@ -248,24 +248,30 @@ def tiny_gqa_decode(seed: int = 0) -> Case:
                      scale=1.0 / 8.0, num_blocks=64, max_blocks_per_seq=16)
 
 
+def _suffix(block_size: int) -> str:
+    return "" if block_size == 16 else f"_bs{block_size}"
+
+
 def llama8b_decode(seed: int = 0, batch: int = 256, max_ctx: int = 4096,
-                   sigma: float = 1.0) -> Case:
+                   sigma: float = 1.0, block_size: int = 16) -> Case:
     """Llama-3.1-8B-shaped decode: 32 query / 8 KV heads, head_dim 128, bf16,
-    block 16, context lengths lognormal (median 400, sigma 1.0) clipped to
-    [16, 4096]."""
+    block 16 (or block_size), context lengths lognormal (median 400,
+    sigma 1.0) clipped to [16, 4096].  The lengths depend on the seed only,
+    not on the block size."""
     rng = np.random.default_rng(seed)
     ctx = np.exp(rng.normal(math.log(400.0), sigma, size=batch))
     ctx = np.clip(np.rint(ctx), 16, max_ctx).astype(np.int64)
-    return make_case("llama8b_decode" if batch == 256 else f"llama8b_decode_b{batch}",
+    name = "llama8b_decode" if batch == 256 else f"llama8b_decode_b{batch}"
+    return make_case(name + _suffix(block_size),
                      seed=seed, rng=rng, dtype=BF16, num_heads=32,
-                     num_kv_heads=8, head_dim=128, block_size=16,
+                     num_kv_heads=8, head_dim=128, block_size=block_size,
                      context_lens=ctx, query_lens=np.ones(batch, np.int64),
-                     max_blocks_per_seq=(max_ctx + 15) // 16)
+                     max_blocks_per_seq=(max_ctx + block_size - 1) // block_size)
 
 
 def mixed_prefill_decode(seed: int = 0, n_prefill: int = 16, n_decode: int = 48,
                          q_range=(32, 512), prior_range=(0, 2048),
-                         dec_range=(64, 4096)) -> Case:
+                         dec_range=(64, 4096), block_size: int = 16) -> Case:
     """Chunked prefill mixed with decode on the Llama-3.1-8B shape: 16
     sequences with query chunks of uniform [32, 512] new tokens after a prior
     context uniform in [0, 2048], and 48 decode sequences (one query token,
@@ -278,9 +284,10 @@ def mixed_prefill_decode(seed: int = 0, n_prefill: int = 16, n_decode: int = 48,
     ql = np.concatenate([qp, np.ones(n_decode, np.int64)])
     order = rng.permutation(n_prefill + n_decode)
     ctx, ql = ctx[order], ql[order]
-    mbs = (max(prior_range[1] + q_range[1], dec_range[1]) + 15) // 16
-    return make_case("mixed_prefill_decode", seed=seed, rng=rng, dtype=BF16,
-                     num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    mbs = (max(prior_range[1] + q_range[1], dec_range[1]) + block_size - 1) // block_size
+    return make_case("mixed_prefill_decode" + _suffix(block_size), seed=seed, rng=rng,
+                     dtype=BF16, num_heads=32, num_kv_heads=8, head_dim=128,
+                     block_size=block_size,
                      context_lens=ctx, query_lens=ql, max_blocks_per_seq=mbs,
                      is_decode=False)
 
