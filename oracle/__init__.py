@@ -55,6 +55,9 @@ def _load():
                                         i32, i32, i32, i64, i32, P, i64, P, P,
                                         i32, P, P, i32]
     lib.orc_paged_attention.restype = i32
+    lib.orc_cross_attention.argtypes = [P, P, P, P, i32, P, P, dbl, i32, i32,
+                                        i32, i32, i32, i64, i32, P, i64, P, P, i32]
+    lib.orc_cross_attention.restype = i32
     lib.orc_lse_combine.argtypes = [P, P, i64, i32, i32, P]
     lib.orc_lse_combine.restype = None
     lib.orc_to_bits_n.argtypes = [P, i64, i32, P]
@@ -149,6 +152,36 @@ def paged_attention(q, k_cache, v_cache, block_tables, cu_query_lens,
     return out64, outb
 
 
+def cross_attention(q, k_cache, v_cache, block_tables, cu_query_lens,
+                    context_lens, scale: float, num_kv_heads: int, dtype: int,
+                    rows: Optional[np.ndarray] = None, num_threads: int = 0):
+    """fp64 cross-attention (no causal mask: every query row of a sequence
+    sees all of its context_lens cached keys) for the query-token rows
+    ``rows`` (default: all).  Returns (out64 [n, Hq, D], out_bits)."""
+    q = _c(q, np.uint16)
+    k_cache = _c(k_cache, np.uint16)
+    v_cache = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_query_lens, np.int32)
+    ctx = _c(context_lens, np.int32)
+    Tq, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and Hkv == num_kv_heads
+    B = ctx.shape[0]
+    mbs = bt.shape[1] if bt.ndim == 2 else 0
+    rows_a = None if rows is None else _c(rows, np.int64)
+    n = Tq if rows_a is None else rows_a.shape[0]
+    out64 = np.zeros((n, Hq, D), np.float64)
+    outb = np.zeros((n, Hq, D), np.uint16)
+    rc = _load().orc_cross_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), mbs, _ptr(cu),
+        _ptr(ctx), float(scale), B, Hq, Hkv, D, bs, NB, dtype, _ptr(rows_a),
+        n, _ptr(out64), _ptr(outb), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle cross_attention failed: {rc}")
+    return out64, outb
+
+
 def lse_combine(part_o: np.ndarray, part_lse: np.ndarray) -> np.ndarray:
     """Combine split partials: part_o [..., S, D], part_lse [..., S]."""
     po = _c(part_o, np.float64)
@@ -166,6 +199,12 @@ def run_case(case, rows: Optional[np.ndarray] = None, num_threads: int = 0):
     Returns (out64, out_bits, k_cache_after, v_cache_after)."""
     kc = case.k_cache.copy()
     vc = case.v_cache.copy()
+    if getattr(case, "cross", False):  # static encoder cache: nothing to write
+        o64, ob = cross_attention(case.q, kc, vc, case.block_tables,
+                                  case.cu_query_lens, case.context_lens, case.scale,
+                                  case.num_kv_heads, case.dtype, rows=rows,
+                                  num_threads=num_threads)
+        return o64, ob, kc, vc
     reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
     o64, ob = paged_attention(case.q, kc, vc, case.block_tables,
                               case.cu_query_lens, case.context_lens, case.scale,

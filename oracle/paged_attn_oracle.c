@@ -477,6 +477,130 @@ int orc_paged_attention(const uint16_t* q, const uint16_t* k_cache,
 }
 
 /*
+ * Cross-attention over a static paged cache, for selected query rows.
+ *
+ * vLLM PR #7448, "[Core] More-efficient cross-attention parallel QKV
+ * computation", opening post: in a cross-attention layer Q comes from the
+ * decoder's hidden states and K, V from the encoder output; during decode
+ * only Q is new, because the encoder sequence is static.  Reading taken
+ * (the page does not spell out the mask): encoder-decoder attention has no
+ * causal mask, so every query row of sequence b attends to all
+ * context_lens[b] cached encoder keys, whatever its position among the
+ * sequence's query rows, and a sequence may carry more query rows than
+ * keys.  The cache, block tables, head map (h / G), scale, empty-context
+ * rule (a zero row) and output rounding are those of orc_paged_attention.
+ *
+ * rows, out64, out_bits: as for orc_paged_attention.
+ */
+int orc_cross_attention(const uint16_t* q, const uint16_t* k_cache,
+                        const uint16_t* v_cache, const int32_t* block_tables,
+                        int mbs, const int32_t* cu_query_lens,
+                        const int32_t* context_lens, double scale, int B,
+                        int Hq, int Hkv, int D, int bs, int64_t NB, int dtype,
+                        const int64_t* rows, int64_t n_rows, double* out64,
+                        uint16_t* out_bits, int num_threads)
+{
+    orc_problem P = {q, k_cache, v_cache, block_tables, cu_query_lens,
+                     context_lens, mbs, B, Hq, Hkv, D, bs, dtype, NB, scale};
+    if (!q || !k_cache || !v_cache || !block_tables || !cu_query_lens ||
+        !context_lens || !out64)
+        return ORC_ERR_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || bs <= 0 ||
+        mbs < 0 || (dtype != ORC_F16 && dtype != ORC_BF16))
+        return ORC_ERR_ARG;
+    if (B > 0 && cu_query_lens[0] != 0)
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        int ql = cu_query_lens[b + 1] - cu_query_lens[b];
+        int ctx = context_lens[b];
+        if (ql < 0 || ctx < 0 || ctx > mbs * bs) /* no ql <= ctx rule here */
+            return ORC_ERR_ARG;
+    }
+    int64_t Tq = B > 0 ? cu_query_lens[B] : 0;
+    if (!rows)
+        n_rows = Tq;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t tok = rows ? rows[r] : r;
+        if (tok < 0 || tok >= Tq)
+            return ORC_ERR_ARG;
+    }
+
+    int64_t n_items = n_rows * Hq;
+    int err = ORC_OK;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#pragma omp parallel
+#endif
+    {
+        int cap = 0;
+        double *Kh = NULL, *Vh = NULL, *s = NULL;
+        double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+        double* o = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!qv || !o) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            err = ORC_ERR_MEM;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t it = 0; it < n_items; ++it) {
+            if (err != ORC_OK)
+                continue;
+            int64_t r = it / Hq;
+            int h = (int)(it % Hq);
+            int64_t tok = rows ? rows[r] : r;
+            int b = orc_seq_of_token(&P, tok);
+            int n = context_lens[b]; /* every encoder key is visible */
+            int64_t ob = (r * Hq + h) * (int64_t)D;
+            if (n == 0) {
+                for (int d = 0; d < D; ++d) {
+                    out64[ob + d] = 0.0;
+                    if (out_bits)
+                        out_bits[ob + d] = 0;
+                }
+                continue;
+            }
+            if (n > cap) {
+                free(Kh); free(Vh); free(s);
+                cap = n;
+                Kh = (double*)malloc(sizeof(double) * (size_t)cap * D);
+                Vh = (double*)malloc(sizeof(double) * (size_t)cap * D);
+                s = (double*)malloc(sizeof(double) * (size_t)cap);
+                if (!Kh || !Vh || !s) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+                    err = ORC_ERR_MEM;
+                    cap = 0;
+                    continue;
+                }
+            }
+            int grc = orc_gather_expanded(&P, b, h, n, Kh, Vh);
+            if (grc != ORC_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+                err = grc;
+                continue;
+            }
+            for (int d = 0; d < D; ++d)
+                qv[d] = orc_value(q[(tok * Hq + h) * (int64_t)D + d], dtype);
+            orc_softmax_attend(qv, Kh, Vh, 0, n, D, scale, s, o);
+            for (int d = 0; d < D; ++d) {
+                out64[ob + d] = o[d];
+                if (out_bits)
+                    out_bits[ob + d] = orc_to_bits(o[d], dtype);
+            }
+        }
+        free(Kh); free(Vh); free(s); free(qv); free(o);
+    }
+    return err;
+}
+
+/*
  * Log-sum-exp combine of S split partials, for n rows of D values:
  *   M = max_s lse_s,  w_s = e^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s.
  * Partials with lse = -inf carry weight 0; a row whose partials are all

@@ -426,3 +426,105 @@ def test_workload_mixed_layout():
     ql = c.query_lens
     assert (ql == 1).sum() == 48 and ((ql >= 32) & (ql <= 512)).sum() == 16
     assert np.all(c.context_lens >= ql)
+
+
+# --------------------------------------------------------------------------
+# cross-attention (static encoder cache, no causal mask)
+# --------------------------------------------------------------------------
+
+def _small_cross(seed=0, B=3, Hq=4, Hkv=2, D=8, bs=4, enc=None, ql=None, dtype=W.BF16):
+    rng = np.random.default_rng(seed)
+    if enc is None:
+        enc = rng.integers(1, 30, size=B)
+    if ql is None:
+        ql = rng.integers(1, 12, size=B)
+    return W.make_cross_case("cross", seed=seed, rng=rng, dtype=dtype, num_heads=Hq,
+                             num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                             encoder_lens=enc, query_lens=ql)
+
+
+def test_cross_brute_force_dense_loop():
+    # includes a sequence with more query rows than encoder tokens
+    c = _small_cross(seed=5, B=3, Hq=6, Hkv=2, enc=np.array([17, 3, 25]),
+                     ql=np.array([4, 9, 1]))
+    o64, _, kc, vc = oracle.run_case(c)
+    Hq, Hkv, D = c.num_heads, c.num_kv_heads, c.head_dim
+    G = Hq // Hkv
+    q = W.bits_to_f32(c.q, c.dtype).astype(np.float64)
+    for b in range(c.num_seqs):
+        K, V = _dense_sequence(c, kc, vc, b)
+        for tok in range(int(c.cu_query_lens[b]), int(c.cu_query_lens[b + 1])):
+            qg = q[tok].reshape(Hkv, G, D)
+            for kvh in range(Hkv):
+                for g in range(G):
+                    s = c.scale * (K[:, kvh] @ qg[kvh, g])       # every key
+                    w = np.exp(s - s.max())
+                    ref = (w[:, None] * V[:, kvh]).sum(0) / w.sum()
+                    np.testing.assert_allclose(o64[tok, kvh * G + g], ref, rtol=0, atol=1e-12)
+
+
+def test_cross_equals_one_decode_row_per_query_token_bitwise():
+    # Without a causal mask, each query row is a decode row (qlen 1, all
+    # keys) over its sequence's cache: the decode definition, pinned above.
+    c = _small_cross(seed=6, B=3)
+    o_cross, _, kc, vc = oracle.run_case(c)
+    ql = np.diff(c.cu_query_lens)
+    seq = np.repeat(np.arange(c.num_seqs), ql)
+    bt = c.block_tables[seq]
+    ctx = c.context_lens[seq]
+    cu = np.arange(len(seq) + 1, dtype=np.int32)
+    o_dec, _ = oracle.paged_attention(c.q, kc, vc, bt, cu, ctx, c.scale,
+                                      c.num_kv_heads, c.dtype)
+    assert np.array_equal(o_cross, o_dec)
+
+
+def test_cross_g1_matches_torch_sdpa_without_mask():
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    c = _small_cross(seed=7, B=3, Hq=4, Hkv=4, D=16, bs=8,
+                     enc=np.array([33, 6, 19]), ql=np.array([5, 11, 1]))
+    o64, _, kc, vc = oracle.run_case(c)
+    q = torch.from_numpy(W.bits_to_f32(c.q, c.dtype).astype(np.float64))
+    for b in range(c.num_seqs):
+        K, V = _dense_sequence(c, kc, vc, b)
+        c0, c1 = int(c.cu_query_lens[b]), int(c.cu_query_lens[b + 1])
+        ref = F.scaled_dot_product_attention(
+            q[c0:c1].permute(1, 0, 2), torch.from_numpy(K).permute(1, 0, 2),
+            torch.from_numpy(V).permute(1, 0, 2), scale=c.scale)
+        np.testing.assert_allclose(o64[c0:c1], ref.permute(1, 0, 2).numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+def test_cross_query_order_is_irrelevant_bitwise():
+    c = _small_cross(seed=8, B=2, ql=np.array([7, 5]))
+    o64, _, kc, vc = oracle.run_case(c)
+    perm = np.concatenate([np.random.default_rng(1).permutation(7),
+                           7 + np.random.default_rng(2).permutation(5)])
+    o_perm, _ = oracle.cross_attention(c.q[perm], kc, vc, c.block_tables,
+                                       c.cu_query_lens, c.context_lens, c.scale,
+                                       c.num_kv_heads, c.dtype)
+    assert np.array_equal(o_perm, o64[perm])
+
+
+def test_cross_empty_encoder_gives_zero_rows_and_reads_nothing():
+    c = _small_cross(seed=9, B=3, enc=np.array([0, 12, 0]), ql=np.array([3, 2, 4]))
+    o64, ob, _, _ = oracle.run_case(c)
+    for b in (0, 2):
+        c0, c1 = int(c.cu_query_lens[b]), int(c.cu_query_lens[b + 1])
+        assert np.all(o64[c0:c1] == 0) and np.all(ob[c0:c1] == 0)
+    assert np.all(np.isfinite(o64))
+
+
+def test_cross_workload_layout():
+    c = W.cross_attention_decode(0)
+    assert c.cross and c.is_decode and c.slot_mapping.size == 0
+    assert set(np.unique(c.context_lens)) <= {1601, 3202, 4803, 6404}
+    p = W.cross_attention_prefill(0)
+    assert p.cross and not p.is_decode
+    assert np.all(np.diff(p.cu_query_lens) >= 32) and np.all(np.diff(p.cu_query_lens) <= 512)
+    # every slot that holds no encoder token is NaN
+    nb = (p.context_lens.astype(np.int64) + p.block_size - 1) // p.block_size
+    used = np.zeros(p.num_blocks, bool)
+    for b in range(p.num_seqs):
+        used[p.block_tables[b, :nb[b]]] = True
+    assert np.all(W.bits_to_f32(p.k_cache[~used], p.dtype) != W.bits_to_f32(p.k_cache[~used], p.dtype))

@@ -105,6 +105,7 @@ class Case:
     cu_query_lens: np.ndarray
     is_decode: bool
     num_splits: int = 0
+    cross: bool = False  # static encoder cache, no causal mask, no new K/V
 
     @property
     def num_seqs(self) -> int:
@@ -233,6 +234,60 @@ def make_case(name: str, *, seed: int, dtype: int, num_heads: int,
                 is_decode=is_decode, num_splits=num_splits)
 
 
+def make_cross_case(name: str, *, seed: int, dtype: int, num_heads: int,
+                    num_kv_heads: int, head_dim: int, block_size: int,
+                    encoder_lens, query_lens, scale: Optional[float] = None,
+                    spare_frac: float = 0.05, max_blocks_per_seq: Optional[int] = None,
+                    rng: Optional[np.random.Generator] = None) -> Case:
+    """A cross-attention step: every sequence's encoder keys and values
+    (``encoder_lens[b]`` tokens) already sit in the paged cache and stay
+    there; the step adds ``query_lens[b]`` decoder query rows (any number,
+    also more than the encoder tokens) and writes no K/V.  Unused blocks and
+    last-block tails are NaN, as in make_case."""
+    if rng is None:
+        rng = np.random.default_rng(seed)
+    ctx = np.asarray(encoder_lens, dtype=np.int64)
+    ql = np.asarray(query_lens, dtype=np.int64)
+    B = ctx.shape[0]
+    assert ql.shape == (B,) and np.all(ql >= 0) and np.all(ctx >= 0)
+    bs = block_size
+    nb = (ctx + bs - 1) // bs
+    need = int(nb.sum())
+    NB = max(1, need + int(math.ceil(spare_frac * need)))
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(1, int(nb.max()) if B else 1)
+    Hkv, D = num_kv_heads, head_dim
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    perm = rng.permutation(NB).astype(np.int32)
+    bt = np.full((B, max_blocks_per_seq), -1, dtype=np.int32)
+    off = 0
+    for b in range(B):
+        bt[b, :nb[b]] = perm[off:off + nb[b]]
+        off += nb[b]
+    k_cache = _normal_bits(rng, (NB, Hkv, bs, D), dtype)
+    v_cache = _normal_bits(rng, (NB, Hkv, bs, D), dtype)
+    valid = np.zeros((NB, bs), dtype=bool)
+    for b in range(B):
+        blocks = bt[b, :nb[b]].astype(np.int64)
+        pos = np.arange(ctx[b], dtype=np.int64)
+        valid.reshape(-1)[blocks[pos // bs] * bs + pos % bs] = True
+    nan = np.uint16(NAN_BITS[dtype])
+    k_cache.transpose(0, 2, 1, 3)[~valid] = nan
+    v_cache.transpose(0, 2, 1, 3)[~valid] = nan
+    Tq = int(ql.sum())
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(ql)
+    q = _normal_bits(rng, (Tq, num_heads, D), dtype)
+    empty = np.zeros((0, Hkv, D), np.uint16)
+    return Case(name=name, dtype=dtype, num_heads=num_heads, num_kv_heads=Hkv,
+                head_dim=D, block_size=bs, scale=float(scale), q=q,
+                k_cache=k_cache, v_cache=v_cache, k_new=empty, v_new=empty.copy(),
+                slot_mapping=np.zeros(0, np.int64), block_tables=bt,
+                context_lens=ctx.astype(np.int32), cu_query_lens=cu,
+                is_decode=bool(np.all(ql == 1)), cross=True)
+
+
 # --------------------------------------------------------------------------
 # Named workloads
 # --------------------------------------------------------------------------
@@ -318,12 +373,46 @@ def long_context_decode(seed: int = 0, batch: int = 8, lo: int = 16384,
                      num_splits=num_splits)
 
 
+# Vision tokens per image of a Llama-3.2-Vision-style encoder: 1601 per
+# image tile (1600 patches and a class token), 1 to 4 tiles.  The page on
+# cross-attention QKV (vLLM PR #7448, discussion) measures that model family
+# at batch 16; the token count is the model's, assumed here.
+_VISION_TOKENS_PER_TILE = 1601
+
+
+def cross_attention_decode(seed: int = 0, batch: int = 16, block_size: int = 16) -> Case:
+    """Cross-attention decode (one decoder token per sequence) over a static
+    encoder cache, Llama-3.2-11B-Vision-shaped cross-attention layer: 32 query
+    / 8 KV heads, head_dim 128, bf16; each sequence's encoder output is 1-4
+    image tiles of 1601 vision tokens (uniform)."""
+    rng = np.random.default_rng(seed)
+    enc = rng.integers(1, 5, size=batch) * _VISION_TOKENS_PER_TILE
+    return make_cross_case("cross_attention_decode" + _suffix(block_size), seed=seed, rng=rng,
+                           dtype=BF16, num_heads=32, num_kv_heads=8, head_dim=128,
+                           block_size=block_size, encoder_lens=enc,
+                           query_lens=np.ones(batch, np.int64))
+
+
+def cross_attention_prefill(seed: int = 0, batch: int = 16, q_range=(32, 512),
+                            block_size: int = 16) -> Case:
+    """The decoder's prompt chunk attending to the same static encoder cache
+    (no causal mask): batch 16, decoder chunks uniform [32, 512] tokens."""
+    rng = np.random.default_rng(seed)
+    enc = rng.integers(1, 5, size=batch) * _VISION_TOKENS_PER_TILE
+    ql = rng.integers(q_range[0], q_range[1] + 1, size=batch)
+    return make_cross_case("cross_attention_prefill" + _suffix(block_size), seed=seed, rng=rng,
+                           dtype=BF16, num_heads=32, num_kv_heads=8, head_dim=128,
+                           block_size=block_size, encoder_lens=enc, query_lens=ql)
+
+
 CONFIGS = {
     "tiny_gqa_decode": tiny_gqa_decode,
     "llama8b_decode": llama8b_decode,
     "mixed_prefill_decode": mixed_prefill_decode,
     "head_sweep": head_sweep,
     "long_context_decode": long_context_decode,
+    "cross_attention_decode": cross_attention_decode,
+    "cross_attention_prefill": cross_attention_prefill,
 }
 
 
