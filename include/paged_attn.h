@@ -170,6 +170,33 @@ PA_API int paged_attn_chunked_prefill(const void* q, const void* k_cache,
                                size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * paged_attn_cross_attention -- attention of decoder query rows over a
+ * static, already written encoder K/V cache (vLLM PR #7448, "[Core]
+ * More-efficient cross-attention parallel QKV computation", opening post:
+ * Q comes from the decoder, K and V from the encoder output, and during
+ * decode the encoder sequence is static, so no new K/V are written).
+ *
+ * Same arguments, layouts, ownership and errors as
+ * paged_attn_chunked_prefill, with two differences: context_lens[b] is the
+ * number of encoder tokens of sequence b in the cache, and there is no
+ * causal mask -- every query row of sequence b attends to all
+ * context_lens[b] keys, whatever its position among the sequence's rows, so
+ * a sequence may carry more query rows than keys.  Sequences with one query
+ * row take the decode path (with KV splits), the others the tensor-core
+ * path; a sequence without encoder tokens gives zero rows.  The workspace
+ * size is paged_attn_chunked_prefill_workspace_bytes.
+ */
+PA_API int paged_attn_cross_attention(const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* cu_query_lens,
+                               const int32_t* context_lens, int total_query_tokens,
+                               int max_query_len, float scale, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, int dtype,
+                               int num_splits, void* out, void* workspace,
+                               size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Read (and clear, if `clear` != 0) the device status word kept in a
  * workspace after the work queued on `stream` so far has finished.  This
  * call synchronises `stream`.  *flags receives PA_DEV_* bits (host pointer).

@@ -58,6 +58,8 @@ _lib.paged_attn_chunked_prefill_workspace_bytes.restype = _SZ
 _lib.paged_attn_chunked_prefill.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, _F, _I, _I,
                                             _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
 _lib.paged_attn_chunked_prefill.restype = _I
+_lib.paged_attn_cross_attention.argtypes = _lib.paged_attn_chunked_prefill.argtypes
+_lib.paged_attn_cross_attention.restype = _I
 _lib.pa_read_device_status.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.pa_read_device_status.restype = _I
 
@@ -71,7 +73,8 @@ EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_l
             "pa_last_cuda_error", "pa_last_cuda_error_string", "reshape_and_cache",
             "paged_attn_workspace_bytes", "paged_attn_decode",
             "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
-            "pa_read_device_status", "paged_attn_decode_noalloc"]
+            "pa_read_device_status", "paged_attn_decode_noalloc",
+            "paged_attn_cross_attention"]
 
 
 class PagedAttnError(RuntimeError):
@@ -205,6 +208,33 @@ def paged_attn_chunked_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         _dtype_code(q), num_splits, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "paged_attn_chunked_prefill")
+    return out
+
+
+def paged_attn_cross_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, cu_query_lens: torch.Tensor,
+                               context_lens: torch.Tensor, max_query_len: int, scale: float,
+                               out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """Decoder rows q [T, Hq, D] (cu_query_lens layout) over a static encoder
+    cache; context_lens = encoder tokens per sequence; no causal mask."""
+    _contig(q, k_cache, v_cache, block_tables, cu_query_lens, context_lens, out)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    B = context_lens.shape[0]
+    mbs = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(paged_attn_chunked_prefill_workspace_bytes(
+            B, T, Hq, Hkv, D, mbs, bs, num_splits), q.device)
+    rc = _lib.paged_attn_cross_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mbs, _ptr(cu_query_lens),
+        _ptr(context_lens), T, int(max_query_len), float(scale), B, Hq, Hkv, D, bs, NB,
+        _dtype_code(q), num_splits, _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "paged_attn_cross_attention")
     return out
 
 

@@ -189,6 +189,137 @@ int finish(int launched) {
 }
 
 }  // namespace
+
+// The chunked path: causal = 1 is paged_attn_chunked_prefill (bottom-right
+// causal chunks), causal = 0 is paged_attn_cross_attention (every query row
+// sees all of its sequence's cached keys).
+int run_chunked(const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, int max_blocks_per_seq,
+                const int32_t* cu_query_lens, const int32_t* context_lens,
+                int total_query_tokens, int max_query_len, float scale,
+                int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                int block_size, int num_blocks, int dtype, int num_splits,
+                void* out, void* workspace, size_t workspace_bytes,
+                pa_stream_t stream, int causal) {
+  g_last_launches = 0;
+  int rc = check_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        scale, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, dtype, num_splits, out);
+  if (rc != PA_OK) return rc;
+  if (total_query_tokens < 0 || max_query_len < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0 || total_query_tokens == 0) return PA_OK;
+  if (!cu_query_lens) return PA_ERR_NULL;
+  const WsLayout L = prefill_layout(num_seqs, total_query_tokens, num_heads, num_kv_heads,
+                     head_dim, max_blocks_per_seq, block_size, num_splits);
+  if ((rc = check_workspace(workspace, workspace_bytes, L)) != PA_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = current_device(dev)) != PA_OK) return rc;
+
+  const int G = num_heads / num_kv_heads;
+  const int TQ = prefill_tokens_per_tile(G);
+  const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
+  CUtensorMap tmk, tmv, tmq;
+  if ((rc = encode_cache_map(&tmk, k_cache, rows, head_dim)) != PA_OK) return rc;
+  if ((rc = encode_cache_map(&tmv, v_cache, rows, head_dim)) != PA_OK) return rc;
+  if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
+      PA_OK)
+    return rc;
+  // The prefill kernel gathers K/V in boxes of gcd(block_size, 64) keys: a
+  // 64-key stage then takes 64 / box_rows boxes per 64 columns, and larger
+  // blocks mean fewer, larger TMA copies.
+  const int box_rows = (block_size % 64 == 0) ? 64 : (block_size % 32 == 0) ? 32 : 16;
+  CUtensorMap tmk_pf = tmk, tmv_pf = tmv;
+  if (box_rows != kKeyTile && max_query_len > 1) {
+    if ((rc = encode_cache_map(&tmk_pf, k_cache, rows, head_dim, box_rows)) != PA_OK) return rc;
+    if ((rc = encode_cache_map(&tmv_pf, v_cache, rows, head_dim, box_rows)) != PA_OK) return rc;
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool bf16 = dtype == PA_BF16;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  PrepareParams pp;
+  pp.context_lens = context_lens;
+  pp.cu_query_lens = cu_query_lens;
+  pp.out = out;
+  pp.hdr = reinterpret_cast<WsHeader*>(ws);
+  pp.seq_info = reinterpret_cast<SeqInfo*>(ws + L.seq_info);
+  pp.pairs = reinterpret_cast<DecPair*>(ws + L.pairs);
+  pp.tiles = reinterpret_cast<PfTile*>(ws + L.tiles);
+  pp.num_seqs = num_seqs;
+  pp.block_size = block_size;
+  pp.num_splits = num_splits;
+  pp.num_kv_heads = num_kv_heads;
+  pp.num_heads = num_heads;
+  pp.head_dim = head_dim;
+  pp.tokens_per_tile = TQ;
+  pp.max_blocks_per_seq = max_blocks_per_seq;
+  pp.total_tokens = total_query_tokens;
+  pp.causal = causal;
+
+  PrefillParams fp;
+  fp.block_tables = block_tables;
+  fp.context_lens = context_lens;
+  fp.out = out;
+  fp.tiles = pp.tiles;
+  fp.hdr = pp.hdr;
+  fp.mbs = max_blocks_per_seq;
+  fp.num_heads = num_heads;
+  fp.num_kv_heads = num_kv_heads;
+  fp.G = G;
+  fp.block_size = block_size;
+  fp.num_blocks = num_blocks;
+  fp.tokens_per_tile = TQ;
+  fp.box_rows = box_rows;
+  fp.causal = causal;
+  fp.scale_log2 = scale * 1.4426950408889634f;
+
+  DecodeParams dp;
+  dp.q = q;
+  dp.block_tables = block_tables;
+  dp.out = out;
+  dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  dp.pairs = pp.pairs;
+  dp.hdr = pp.hdr;
+  dp.mbs = max_blocks_per_seq;
+  dp.num_heads = num_heads;
+  dp.num_kv_heads = num_kv_heads;
+  dp.G = G;
+  dp.block_size = block_size;
+  dp.num_blocks = num_blocks;
+  dp.scale_log2 = fp.scale_log2;
+
+
+  const ProfileScope prof(st);
+  int n = 0, r;
+  if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
+  n += r;
+  prof.begin();
+  if (max_query_len > 1) {
+    if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
+                dev.num_sms)) < 0)
+      return cuda_error();
+    n += r;
+  }
+  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return cuda_error();
+  n += r;
+  prof.end();
+  if (num_splits != 1) {
+    CombineParams cp;
+    cp.seq_info = pp.seq_info;
+    cp.part_o = dp.part_o;
+    cp.part_lse = dp.part_lse;
+    cp.out = out;
+    cp.num_seqs = num_seqs;
+    cp.num_heads = num_heads;
+    cp.head_dim = head_dim;
+    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
+    n += r;
+  }
+  return finish(n);
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -301,6 +432,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   pp.tokens_per_tile = prefill_tokens_per_tile(G);
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.total_tokens = num_seqs;
+  pp.causal = 1;
 
   DecodeParams dp;
   dp.q = q;
@@ -362,121 +494,24 @@ int paged_attn_chunked_prefill(const void* q, const void* k_cache, const void* v
                                int block_size, int num_blocks, int dtype, int num_splits,
                                void* out, void* workspace, size_t workspace_bytes,
                                pa_stream_t stream) {
-  g_last_launches = 0;
-  int rc = check_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                        scale, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                        num_blocks, dtype, num_splits, out);
-  if (rc != PA_OK) return rc;
-  if (total_query_tokens < 0 || max_query_len < 0) return PA_ERR_SHAPE;
-  if (num_seqs == 0 || total_query_tokens == 0) return PA_OK;
-  if (!cu_query_lens) return PA_ERR_NULL;
-  const WsLayout L = prefill_layout(num_seqs, total_query_tokens, num_heads, num_kv_heads,
-                                    head_dim, max_blocks_per_seq, block_size, num_splits);
-  if ((rc = check_workspace(workspace, workspace_bytes, L)) != PA_OK) return rc;
-  DeviceInfo dev;
-  if ((rc = current_device(dev)) != PA_OK) return rc;
+  return pa::run_chunked(q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_query_lens,
+                         context_lens, total_query_tokens, max_query_len, scale, num_seqs,
+                         num_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype,
+                         num_splits, out, workspace, workspace_bytes, stream, 1);
+}
 
-  const int G = num_heads / num_kv_heads;
-  const int TQ = prefill_tokens_per_tile(G);
-  const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
-  CUtensorMap tmk, tmv, tmq;
-  if ((rc = encode_cache_map(&tmk, k_cache, rows, head_dim)) != PA_OK) return rc;
-  if ((rc = encode_cache_map(&tmv, v_cache, rows, head_dim)) != PA_OK) return rc;
-  if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
-      PA_OK)
-    return rc;
-  // The prefill kernel gathers K/V in boxes of gcd(block_size, 64) keys: a
-  // 64-key stage then takes 64 / box_rows boxes per 64 columns, and larger
-  // blocks mean fewer, larger TMA copies.
-  const int box_rows = (block_size % 64 == 0) ? 64 : (block_size % 32 == 0) ? 32 : 16;
-  CUtensorMap tmk_pf = tmk, tmv_pf = tmv;
-  if (box_rows != kKeyTile && max_query_len > 1) {
-    if ((rc = encode_cache_map(&tmk_pf, k_cache, rows, head_dim, box_rows)) != PA_OK) return rc;
-    if ((rc = encode_cache_map(&tmv_pf, v_cache, rows, head_dim, box_rows)) != PA_OK) return rc;
-  }
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const bool bf16 = dtype == PA_BF16;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-  PrepareParams pp;
-  pp.context_lens = context_lens;
-  pp.cu_query_lens = cu_query_lens;
-  pp.out = out;
-  pp.hdr = reinterpret_cast<WsHeader*>(ws);
-  pp.seq_info = reinterpret_cast<SeqInfo*>(ws + L.seq_info);
-  pp.pairs = reinterpret_cast<DecPair*>(ws + L.pairs);
-  pp.tiles = reinterpret_cast<PfTile*>(ws + L.tiles);
-  pp.num_seqs = num_seqs;
-  pp.block_size = block_size;
-  pp.num_splits = num_splits;
-  pp.num_kv_heads = num_kv_heads;
-  pp.num_heads = num_heads;
-  pp.head_dim = head_dim;
-  pp.tokens_per_tile = TQ;
-  pp.max_blocks_per_seq = max_blocks_per_seq;
-  pp.total_tokens = total_query_tokens;
-
-  PrefillParams fp;
-  fp.block_tables = block_tables;
-  fp.context_lens = context_lens;
-  fp.out = out;
-  fp.tiles = pp.tiles;
-  fp.hdr = pp.hdr;
-  fp.mbs = max_blocks_per_seq;
-  fp.num_heads = num_heads;
-  fp.num_kv_heads = num_kv_heads;
-  fp.G = G;
-  fp.block_size = block_size;
-  fp.num_blocks = num_blocks;
-  fp.tokens_per_tile = TQ;
-  fp.box_rows = box_rows;
-  fp.scale_log2 = scale * 1.4426950408889634f;
-
-  DecodeParams dp;
-  dp.q = q;
-  dp.block_tables = block_tables;
-  dp.out = out;
-  dp.part_o = reinterpret_cast<float*>(ws + L.part_o);
-  dp.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
-  dp.pairs = pp.pairs;
-  dp.hdr = pp.hdr;
-  dp.mbs = max_blocks_per_seq;
-  dp.num_heads = num_heads;
-  dp.num_kv_heads = num_kv_heads;
-  dp.G = G;
-  dp.block_size = block_size;
-  dp.num_blocks = num_blocks;
-  dp.scale_log2 = fp.scale_log2;
-
-
-  const ProfileScope prof(st);
-  int n = 0, r;
-  if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
-  n += r;
-  prof.begin();
-  if (max_query_len > 1) {
-    if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
-                               dev.num_sms)) < 0)
-      return cuda_error();
-    n += r;
-  }
-  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return cuda_error();
-  n += r;
-  prof.end();
-  if (num_splits != 1) {
-    CombineParams cp;
-    cp.seq_info = pp.seq_info;
-    cp.part_o = dp.part_o;
-    cp.part_lse = dp.part_lse;
-    cp.out = out;
-    cp.num_seqs = num_seqs;
-    cp.num_heads = num_heads;
-    cp.head_dim = head_dim;
-    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
-    n += r;
-  }
-  return finish(n);
+int paged_attn_cross_attention(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* cu_query_lens, const int32_t* context_lens,
+                               int total_query_tokens, int max_query_len, float scale,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, int dtype, int num_splits,
+                               void* out, void* workspace, size_t workspace_bytes,
+                               pa_stream_t stream) {
+  return pa::run_chunked(q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_query_lens,
+                         context_lens, total_query_tokens, max_query_len, scale, num_seqs,
+                         num_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype,
+                         num_splits, out, workspace, workspace_bytes, stream, 0);
 }
 
 int pa_read_device_status(const void* workspace, int clear, uint32_t* flags, pa_stream_t stream) {

@@ -57,6 +57,8 @@ struct PfTile {
   int32_t tok0;   // first query row of the tile
   int32_t ntok;   // valid query tokens in the tile
   int32_t pos0;   // absolute position of the first token (ctx - qlen + i)
+  int32_t nkv;    // keys the tile reads: pos0 + ntok (causal) or ctx (cross)
+  int32_t pad[3];
 };
 
 struct WsLayout {
@@ -115,6 +117,7 @@ struct PrepareParams {
   int num_seqs, block_size, num_splits, num_kv_heads, num_heads, head_dim;
   int tokens_per_tile;  // prefill tile height in tokens
   int max_blocks_per_seq;
+  int causal;           // 0: cross-attention, every row sees all keys, qlen may exceed ctx
   int64_t total_tokens;  // rows of q / out
 };
 
@@ -147,6 +150,7 @@ struct PrefillParams {
   WsHeader* hdr;
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks, tokens_per_tile;
   int box_rows;  // keys per K/V box: gcd(block_size, 64), so a box never crosses a block
+  int causal;    // 0: cross-attention (every row sees all of the tile's keys)
   float scale_log2;
 };
 

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t ti = it / static_cast<uint32_t>(Hkv);
       const int kvh = static_cast<int>(it - ti * static_cast<uint32_t>(Hkv));
       const PfTile tile = p.tiles[ti];
-      const int nkv = tile.pos0 + tile.ntok;
+      const int nkv = tile.nkv;
       if (lane == 0) {
         TcMeta m;
         m.tok0 = tile.tok0;
@@ -398,7 +398,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(&bar[kBarQEmpty]);
       const int tl = t * TQ + row / G;  // token within the pair
       const bool valid = row < rows_used && tl < m.ntok;
-      const int pos = m.pos0 + tl;
+      // causal: the row's absolute position; cross-attention: every key
+      const int pos = p.causal ? m.pos0 + tl : m.nkv - 1;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;

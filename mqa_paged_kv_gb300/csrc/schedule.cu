@@ -40,7 +40,7 @@ __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
   }
   const int ctx = s.ctx;
   const int max_ctx = p.max_blocks_per_seq * p.block_size;
-  if (ctx < 0 || ctx > max_ctx || s.qlen < 0 || (s.qlen > ctx && ctx > 0) || s.tok < 0 ||
+  if (ctx < 0 || ctx > max_ctx || s.qlen < 0 || (p.causal && s.qlen > ctx && ctx > 0) || s.tok < 0 ||
       static_cast<int64_t>(s.tok) + s.qlen > p.total_tokens) {
     s.bad = true;
     s.qlen = 0;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
       for (int t = 0; t < s.ntile; ++t) {
         const int ntok = min(s.qlen - t * p.tokens_per_tile, p.tokens_per_tile);
         const int pos0 = s.ctx - s.qlen + t * p.tokens_per_tile;
-        atomicAdd(&pf_cnt[pf_bucket(pos0 + ntok)], 1);
+        atomicAdd(&pf_cnt[pf_bucket(p.causal ? pos0 + ntok : s.ctx)], 1);
       }
     }
     // Decode splits: all but the last have the full chunk length.
@@ -221,7 +221,9 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
       tl.tok0 = s.tok + t * p.tokens_per_tile;
       tl.ntok = min(s.qlen - t * p.tokens_per_tile, p.tokens_per_tile);
       tl.pos0 = s.ctx - s.qlen + t * p.tokens_per_tile;
-      const int pos = atomicAdd(&pf_cnt[pf_bucket(tl.pos0 + tl.ntok)], 1);
+      tl.nkv = p.causal ? tl.pos0 + tl.ntok : s.ctx;
+      tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+      const int pos = atomicAdd(&pf_cnt[pf_bucket(tl.nkv)], 1);
       p.tiles[pos] = tl;
     }
     if (s.ctx == 0 && s.qlen > 0 && p.out) {

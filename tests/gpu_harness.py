@@ -42,12 +42,25 @@ class GpuCase:
         self.workspace = None
 
     def write_cache(self):
+        if getattr(self.case, "cross", False):  # static encoder cache
+            return
         self.pa.reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache,
                                   self.slot_mapping)
 
     def attention(self, num_splits=0, out=None, force_chunked=False):
         c, pa = self.case, self.pa
         B, Hq, D = c.num_seqs, c.num_heads, c.head_dim
+        if getattr(c, "cross", False):
+            nb = pa.paged_attn_chunked_prefill_workspace_bytes(
+                B, c.total_query_tokens, Hq, c.num_kv_heads, D, c.max_blocks_per_seq,
+                c.block_size, num_splits)
+            if self.workspace is None or self.workspace.numel() < nb:
+                self.workspace = pa.alloc_workspace(nb, self.q.device)
+            return pa.paged_attn_cross_attention(self.q, self.k_cache, self.v_cache,
+                                                 self.block_tables, self.cu_query_lens,
+                                                 self.context_lens, c.max_query_len, c.scale,
+                                                 out=out, num_splits=num_splits,
+                                                 workspace=self.workspace)
         if c.is_decode and not force_chunked:
             nb = pa.paged_attn_workspace_bytes(B, Hq, c.num_kv_heads, D,
                                                c.max_blocks_per_seq, c.block_size, num_splits)
