@@ -54,7 +54,8 @@ def parse_args():
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "mixed_prefill_decode", "head_sweep_kv1",
                              "head_sweep_kv8", "head_sweep_kv32", "long_context_decode",
-                             "tiny_gqa_decode"])
+                             "tiny_gqa_decode", "cross_attention_decode",
+                             "cross_attention_prefill"])
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the mixed-batch line item")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -70,8 +71,10 @@ def make_workload(name: str, seed: int, block_size: int = 16):
     if name.startswith("head_sweep_kv"):
         return W.head_sweep(seed, num_kv_heads=int(name[len("head_sweep_kv"):]))
     if block_size != 16:
-        if name not in ("llama8b_decode", "mixed_prefill_decode"):
-            raise SystemExit("--block-size applies to llama8b_decode and mixed_prefill_decode")
+        if name not in ("llama8b_decode", "mixed_prefill_decode", "cross_attention_decode",
+                        "cross_attention_prefill"):
+            raise SystemExit("--block-size applies to llama8b_decode, mixed_prefill_decode "
+                             "and the cross_attention workloads")
         return W.CONFIGS[name](seed, block_size=block_size)
     return W.CONFIGS[name](seed)
 
@@ -96,13 +99,17 @@ def measured_bf16_peak():
 
 
 def prefill_flops(case) -> float:
-    """QK^T and PV of the query chunks (qlen > 1): 4 * Hq * D per visible key."""
+    """QK^T and PV of the query chunks (qlen > 1): 4 * Hq * D per visible key
+    (causal: token i of a chunk sees ctx - qlen + i + 1 keys; cross-attention:
+    every row sees all ctx keys)."""
     ql = np.asarray(case.query_lens, dtype=np.int64)
     cl = np.asarray(case.context_lens, dtype=np.int64)
+    cross = getattr(case, "cross", False)
     total = 0.0
     for q, c in zip(ql, cl):
-        if q > 1:  # token i of the chunk sees c - q + i + 1 keys
-            total += 4.0 * case.num_heads * case.head_dim * float(q * (c - q) + q * (q + 1) // 2)
+        if q > 1:
+            keys = q * c if cross else q * (c - q) + q * (q + 1) // 2
+            total += 4.0 * case.num_heads * case.head_dim * float(keys)
     return total
 
 
@@ -319,7 +326,7 @@ class Step:
             "context_lens": dev(case.context_lens), "cu_query_lens": dev(case.cu_query_lens),
         }
         self.out = torch.empty_like(self.inputs["q"])
-        if case.is_decode:
+        if case.is_decode and not case.cross:
             nb = pa.paged_attn_workspace_bytes(case.num_seqs, case.num_heads,
                                                case.num_kv_heads, case.head_dim,
                                                case.max_blocks_per_seq, case.block_size, splits)
@@ -333,12 +340,20 @@ class Step:
     def run(self, x=None, prof=None):
         pa, c = self.pa, self.case
         x = x or self.inputs
-        pa.reshape_and_cache(x["k_new"], x["v_new"], self.k_cache, self.v_cache,
-                             x["slot_mapping"])
-        n = pa.last_launch_count()
+        n = 0
+        if not c.cross:  # a cross-attention encoder cache is static: nothing to write
+            pa.reshape_and_cache(x["k_new"], x["v_new"], self.k_cache, self.v_cache,
+                                 x["slot_mapping"])
+            n = pa.last_launch_count()
         if prof is not None:
             pa.pa_profile_next_call(*prof)
-        if c.is_decode:
+        if c.cross:
+            pa.paged_attn_cross_attention(x["q"], self.k_cache, self.v_cache,
+                                          x["block_tables"], x["cu_query_lens"],
+                                          x["context_lens"], c.max_query_len, c.scale,
+                                          out=self.out, num_splits=self.splits,
+                                          workspace=self.ws)
+        elif c.is_decode:
             pa.paged_attn_decode(x["q"], self.k_cache, self.v_cache, x["block_tables"],
                                  x["context_lens"], c.scale, out=self.out,
                                  num_splits=self.splits, workspace=self.ws)
@@ -470,12 +485,21 @@ def run_ours(args):
     value = kvb * world / step_s / 1e9
     peak, peak_src = measured_hbm_peak()
     achieved = kvb / kern_s / 1e9
-    if case.is_decode:
+    if case.is_decode:  # also cross-attention decode: the same decode kernel
         traffic = ncu_traffic("decode_kernel", "decode.cu", case.name)
         roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                     "frac": achieved / peak, "kernel_ms": kern_s * 1e3,
                     "algorithmic_bytes": kvb, "traffic": traffic}
+    elif case.cross:  # every sequence carries a chunk: the call is the prefill kernel
+        flops = prefill_flops(case)
+        bpeak, bsrc = measured_bf16_peak()
+        ach = flops / kern_s / 1e12
+        roofline = {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": ach,
+                    "peak": bpeak, "peak_source": bsrc, "unit": "TFLOP/s",
+                    "frac": ach / bpeak, "kernel_ms": kern_s * 1e3,
+                    "algorithmic_flops": flops,
+                    "traffic": ncu_traffic("prefill_tc_kernel", "prefill_tc.cu", case.name)}
     else:
         roofline = prefill_roofline(args.workload, args.seed + rank, device, args, flush)
 
@@ -487,7 +511,8 @@ def run_ours(args):
         "config": dict(W.describe(case), splits=args.splits or "auto",
                        l2=f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB read sweep)",
                        parallelism="replicas" if world > 1 else "single GPU",
-                       step="reshape_and_cache + paged attention",
+                       step=("cross-attention over the static encoder cache" if case.cross
+                             else "reshape_and_cache + paged attention"),
                        step_time_stats=step_stats),
         "hbm_peak_frac": value / world / peak,
         "tokens_per_s": case.total_query_tokens * world / step_s,
