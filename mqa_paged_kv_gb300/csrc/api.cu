@@ -289,6 +289,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   dp.block_size = block_size;
   dp.num_blocks = num_blocks;
   dp.scale_log2 = fp.scale_log2;
+  dp.trigger_dependents = num_splits != 1;
 
 
   const ProfileScope prof(st);
@@ -449,6 +450,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   dp.block_size = block_size;
   dp.num_blocks = num_blocks;
   dp.scale_log2 = scale * 1.4426950408889634f;
+  dp.trigger_dependents = num_splits != 1;
 
 
   const ProfileScope prof(st);

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   fence_proxy_async();
   __syncthreads();
   griddep_wait();  // the work list is written by the preceding kernel
-  griddep_launch_dependents();  // let the split combine become resident
+  if (p.trigger_dependents) griddep_launch_dependents();  // the split combine may become resident
 
   const uint32_t num_items = p.hdr->decode_items;
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
@@ -434,25 +434,29 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
-// Merge the split partials of each decode sequence (one CTA per sequence,
-// one warp per query head):
+// Merge the split partials of each decode sequence (one CTA per sequence
+// and group of kCombineHeads query heads, one warp per head):
 //   M = max_s lse_s, w_s = 2^(lse_s - M), out = sum_s w_s o_s / sum_s w_s,
 // with lse in base 2 and splits of lse = -inf weighted 0.  Latency-bound by
 // design: all loads of a head are issued before any is used.
+// The CTAs are small (4 warps) so that they fit on an SM beside a decode
+// CTA and become resident, waiting, while the decode kernel still runs.
+constexpr int kCombineHeads = 4;
+
 template <bool kBF16, int D>
-__global__ void __launch_bounds__(1024) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(32 * kCombineHeads) combine_kernel(const CombineParams p) {
   griddep_wait();  // partials are written by the decode kernel
   const int b = blockIdx.x;
   const SeqInfo si = p.seq_info[b];
   if (si.qlen != 1 || si.nsplit <= 1) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
+  const int h0 = blockIdx.y * kCombineHeads;
   const int Hq = p.num_heads, S = si.nsplit;
   constexpr int kV = D / 32;  // floats per lane
   const float* lse = p.part_lse + static_cast<int64_t>(si.split_offset) * Hq;
   const float* po = p.part_o + static_cast<int64_t>(si.split_offset) * Hq * D;
   uint16_t* out = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(si.tok) * Hq * D;
-  for (int h = warp; h < Hq; h += nwarps) {
+  for (int h = h0 + warp; h < Hq && h < h0 + kCombineHeads; h += kCombineHeads) {
     // Issue the log-sum-exps and the first eight partial rows together.
     auto load_part = [&](int sp, float (&dst)[kV]) {
       const float* src = po + (static_cast<int64_t>(sp) * Hq + h) * D + lane * kV;
@@ -575,8 +579,9 @@ int launch_decode_d(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
 int launch_combine(const CombineParams& p, bool bf16, int head_dim, cudaStream_t stream) {
   if (p.num_seqs <= 0) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_seqs);
-  cfg.blockDim = dim3(32 * (p.num_heads < 32 ? p.num_heads : 32));
+  const int heads = p.num_heads < kCombineHeads ? p.num_heads : kCombineHeads;
+  cfg.gridDim = dim3(p.num_seqs, (p.num_heads + kCombineHeads - 1) / kCombineHeads);
+  cfg.blockDim = dim3(32 * heads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -132,6 +132,9 @@ struct DecodeParams {
   uint32_t* done;
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks;
   float scale_log2;  // scale * log2(e)
+  // 1 when the split combine follows: only then may the next launch start
+  // early (a following call's work-list build must not overlap this kernel).
+  int trigger_dependents;
 };
 
 struct CombineParams {

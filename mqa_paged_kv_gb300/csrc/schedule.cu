@@ -130,7 +130,13 @@ __device__ __forceinline__ int block_scan(int v, int* warp_sums, int& excl) {
 
 __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   griddep_launch_dependents();  // the attention kernel may start its prologue
-  griddep_wait();               // lengths may come from the previous kernel
+  // The lengths this kernel reads are final before the previous kernel
+  // could let it start early: a kernel of the caller triggers this launch
+  // only when it completes, and the library's own cache write (the one
+  // kernel that triggers early) waits for its predecessors before it does.
+  // So the work list is built while a preceding cache write still runs, and
+  // the wait at the end only orders this kernel's completion after it: the
+  // attention kernels, which wait for this one, then read a complete cache.
 
   __shared__ int warp_sums[kWarps];
   __shared__ int dec_cnt[kDecBuckets];
@@ -243,6 +249,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     h->prefill_tiles = static_cast<uint32_t>(tile_total);
     h->prefill_items = static_cast<uint32_t>(tile_total) * static_cast<uint32_t>(p.num_kv_heads);
   }
+  griddep_wait();
 }
 
 int launch_prepare(const PrepareParams& p, bool /*bf16*/, cudaStream_t stream) {
