@@ -58,6 +58,9 @@ def _load():
     lib.orc_cross_attention.argtypes = [P, P, P, P, i32, P, P, dbl, i32, i32,
                                         i32, i32, i32, i64, i32, P, i64, P, P, i32]
     lib.orc_cross_attention.restype = i32
+    lib.orc_varlen_attention.argtypes = [P, P, P, P, P, dbl, i32, i32, i32, i32, i32,
+                                         P, i64, P, P, i32]
+    lib.orc_varlen_attention.restype = i32
     lib.orc_lse_combine.argtypes = [P, P, i64, i32, i32, P]
     lib.orc_lse_combine.restype = None
     lib.orc_to_bits_n.argtypes = [P, i64, i32, P]
@@ -179,6 +182,29 @@ def cross_attention(q, k_cache, v_cache, block_tables, cu_query_lens,
         n, _ptr(out64), _ptr(outb), int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle cross_attention failed: {rc}")
+    return out64, outb
+
+
+def varlen_attention(q, k, v, cu_q, cu_k, scale: float, dtype: int,
+                     rows: Optional[np.ndarray] = None, num_threads: int = 0):
+    """fp64 GQA prefill over contiguous K/V of a varlen batch: q [Tq, Hq, D],
+    k, v [Tk, Hkv, D], bottom-right causal per sequence.  Returns
+    (out64 [n, Hq, D], out_bits)."""
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    cq, ck = _c(cu_q, np.int32), _c(cu_k, np.int32)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, D2 = k.shape
+    assert D2 == D and v.shape == k.shape and cq.shape == ck.shape
+    B = cq.shape[0] - 1
+    rows_a = None if rows is None else _c(rows, np.int64)
+    n = Tq if rows_a is None else rows_a.shape[0]
+    out64 = np.zeros((n, Hq, D), np.float64)
+    outb = np.zeros((n, Hq, D), np.uint16)
+    rc = _load().orc_varlen_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
+                                      float(scale), B, Hq, Hkv, D, dtype, _ptr(rows_a), n,
+                                      _ptr(out64), _ptr(outb), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle varlen_attention failed: {rc}")
     return out64, outb
 
 

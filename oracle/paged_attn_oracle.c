@@ -601,6 +601,121 @@ int orc_cross_attention(const uint16_t* q, const uint16_t* k_cache,
 }
 
 /*
+ * GQA prefill over contiguous (not paged) keys and values of a varlen batch.
+ *
+ * vLLM issue #1880, "[Performance] Use optimized kernels for MQA/GQA",
+ * item 1: for prefill the incoming keys and values [T, Hkv, D] are expanded
+ * to [T, Hkv, G, D] (a broadcast of each KV head to its G query heads) and
+ * handed to a multi-head attention op.  That is the definition computed
+ * here, literally: the batch holds B sequences whose query rows are
+ * q[cu_q[b] .. cu_q[b+1]) and whose key/value rows are
+ * k, v[cu_k[b] .. cu_k[b+1]); each KV row is expanded to the Hq heads (head
+ * h reads KV head h / G) and every query row attends, causally, to its own
+ * sequence's keys.  Causal alignment as in orc_paged_attention
+ * (bottom-right: with klen keys and qlen query rows, query row t sits at
+ * position klen - qlen + t and sees keys 0..that); klen >= qlen.  With
+ * cu_q == cu_k this is plain causal self-attention over each prompt.
+ *
+ * rows, out64, out_bits: as for orc_paged_attention (rows index q).
+ */
+int orc_varlen_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const int32_t* cu_q, const int32_t* cu_k, double scale,
+                         int B, int Hq, int Hkv, int D, int dtype,
+                         const int64_t* rows, int64_t n_rows, double* out64,
+                         uint16_t* out_bits, int num_threads)
+{
+    if (!q || !k || !v || !cu_q || !cu_k || !out64)
+        return ORC_ERR_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 ||
+        (dtype != ORC_F16 && dtype != ORC_BF16))
+        return ORC_ERR_ARG;
+    if (B > 0 && (cu_q[0] != 0 || cu_k[0] != 0))
+        return ORC_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        int ql = cu_q[b + 1] - cu_q[b], kl = cu_k[b + 1] - cu_k[b];
+        if (ql < 0 || kl < ql)
+            return ORC_ERR_ARG;
+    }
+    int64_t Tq = B > 0 ? cu_q[B] : 0;
+    if (!rows)
+        n_rows = Tq;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t tok = rows ? rows[r] : r;
+        if (tok < 0 || tok >= Tq)
+            return ORC_ERR_ARG;
+    }
+    const int G = Hq / Hkv;
+    int64_t n_items = n_rows * Hq;
+    int err = ORC_OK;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#pragma omp parallel
+#endif
+    {
+        int cap = 0;
+        double *Kh = NULL, *Vh = NULL, *s = NULL;
+        double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+        double* o = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!qv || !o) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            err = ORC_ERR_MEM;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t it = 0; it < n_items; ++it) {
+            if (err != ORC_OK)
+                continue;
+            int64_t r = it / Hq;
+            int h = (int)(it % Hq);
+            int64_t tok = rows ? rows[r] : r;
+            int b = 0; /* sequence owning query row tok */
+            while (b < B - 1 && cu_q[b + 1] <= tok)
+                ++b;
+            int qlen = cu_q[b + 1] - cu_q[b], klen = cu_k[b + 1] - cu_k[b];
+            int n = klen - qlen + (int)(tok - cu_q[b]) + 1; /* keys 0..position */
+            if (n > cap) {
+                free(Kh); free(Vh); free(s);
+                cap = n;
+                Kh = (double*)malloc(sizeof(double) * (size_t)cap * D);
+                Vh = (double*)malloc(sizeof(double) * (size_t)cap * D);
+                s = (double*)malloc(sizeof(double) * (size_t)cap);
+                if (!Kh || !Vh || !s) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+                    err = ORC_ERR_MEM;
+                    cap = 0;
+                    continue;
+                }
+            }
+            /* the expansion: query head h reads KV head h / G of each row */
+            for (int j = 0; j < n; ++j) {
+                int64_t src = ((int64_t)(cu_k[b] + j) * Hkv + h / G) * D;
+                for (int d = 0; d < D; ++d) {
+                    Kh[(int64_t)j * D + d] = orc_value(k[src + d], dtype);
+                    Vh[(int64_t)j * D + d] = orc_value(v[src + d], dtype);
+                }
+            }
+            for (int d = 0; d < D; ++d)
+                qv[d] = orc_value(q[(tok * Hq + h) * (int64_t)D + d], dtype);
+            orc_softmax_attend(qv, Kh, Vh, 0, n, D, scale, s, o);
+            int64_t ob = (r * Hq + h) * (int64_t)D;
+            for (int d = 0; d < D; ++d) {
+                out64[ob + d] = o[d];
+                if (out_bits)
+                    out_bits[ob + d] = orc_to_bits(o[d], dtype);
+            }
+        }
+        free(Kh); free(Vh); free(s); free(qv); free(o);
+    }
+    return err;
+}
+
+/*
  * Log-sum-exp combine of S split partials, for n rows of D values:
  *   M = max_s lse_s,  w_s = e^(lse_s - M),  out = sum_s w_s o_s / sum_s w_s.
  * Partials with lse = -inf carry weight 0; a row whose partials are all

@@ -528,3 +528,104 @@ def test_cross_workload_layout():
     for b in range(p.num_seqs):
         used[p.block_tables[b, :nb[b]]] = True
     assert np.all(W.bits_to_f32(p.k_cache[~used], p.dtype) != W.bits_to_f32(p.k_cache[~used], p.dtype))
+
+
+# --------------------------------------------------------------------------
+# GQA prefill over contiguous varlen K/V (no cache)
+# --------------------------------------------------------------------------
+
+def _varlen(seed=0, Hq=4, Hkv=2, D=8, ql=(5, 1, 9), kl=None, dtype=W.BF16):
+    return W.make_varlen_case("varlen", seed=seed, dtype=dtype, num_heads=Hq,
+                              num_kv_heads=Hkv, head_dim=D, q_lens=ql, k_lens=kl)
+
+
+def test_varlen_literal_expand_then_mha():
+    # the issue's prefill: k[:, :, None, :].expand(T, Hkv, G, D) flattened to
+    # [T, Hq, D], then causal multi-head attention per sequence
+    c = _varlen(seed=1, Hq=6, Hkv=2, ql=(7, 3, 1), kl=(7, 8, 4))
+    o64, _ = oracle.varlen_attention(c.q, c.k, c.v, c.cu_q, c.cu_k, c.scale, c.dtype)
+    G = c.num_heads // c.num_kv_heads
+    q = W.bits_to_f32(c.q, c.dtype).astype(np.float64)
+    k = W.bits_to_f32(c.k, c.dtype).astype(np.float64)
+    v = W.bits_to_f32(c.v, c.dtype).astype(np.float64)
+    ke = np.broadcast_to(k[:, :, None, :], (k.shape[0], c.num_kv_heads, G, c.head_dim))
+    ve = np.broadcast_to(v[:, :, None, :], ke.shape)
+    ke = ke.reshape(k.shape[0], c.num_heads, c.head_dim)
+    ve = ve.reshape(k.shape[0], c.num_heads, c.head_dim)
+    for b in range(c.num_seqs):
+        q0, q1 = int(c.cu_q[b]), int(c.cu_q[b + 1])
+        k0, k1 = int(c.cu_k[b]), int(c.cu_k[b + 1])
+        for t in range(q1 - q0):
+            p = (k1 - k0) - (q1 - q0) + t
+            for h in range(c.num_heads):
+                s = c.scale * (ke[k0:k0 + p + 1, h] @ q[q0 + t, h])
+                w = np.exp(s - s.max())
+                ref = (w[:, None] * ve[k0:k0 + p + 1, h]).sum(0) / w.sum()
+                np.testing.assert_allclose(o64[q0 + t, h], ref, rtol=0, atol=1e-12)
+
+
+def test_varlen_equals_paged_oracle_on_the_same_rows_bitwise():
+    # K/V laid into a paged cache (block 4, blocks in a shuffled order) give
+    # the same numbers through the paged definition
+    c = _varlen(seed=2, Hq=4, Hkv=2, ql=(6, 2, 11), kl=(9, 2, 14))
+    o_var, _ = oracle.varlen_attention(c.q, c.k, c.v, c.cu_q, c.cu_k, c.scale, c.dtype)
+    bs = 4
+    kl = np.diff(c.cu_k)
+    nb = (kl + bs - 1) // bs
+    NB = int(nb.sum())
+    perm = np.random.default_rng(3).permutation(NB).astype(np.int32)
+    bt = np.full((c.num_seqs, int(nb.max())), -1, np.int32)
+    kc = np.full((NB, c.num_kv_heads, bs, c.head_dim), W.NAN_BITS[c.dtype], np.uint16)
+    vc = kc.copy()
+    off = 0
+    for b in range(c.num_seqs):
+        bt[b, :nb[b]] = perm[off:off + nb[b]]
+        off += nb[b]
+        for j in range(kl[b]):
+            kc[bt[b, j // bs], :, j % bs] = c.k[c.cu_k[b] + j]
+            vc[bt[b, j // bs], :, j % bs] = c.v[c.cu_k[b] + j]
+    o_pag, _ = oracle.paged_attention(c.q, kc, vc, bt, c.cu_q, kl.astype(np.int32), c.scale,
+                                      c.num_kv_heads, c.dtype)
+    assert np.array_equal(o_var, o_pag)
+
+
+def test_varlen_g1_matches_torch_sdpa_causal():
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    c = _varlen(seed=4, Hq=4, Hkv=4, D=16, ql=(12, 5), kl=(12, 9))
+    o64, _ = oracle.varlen_attention(c.q, c.k, c.v, c.cu_q, c.cu_k, c.scale, c.dtype)
+    q = torch.from_numpy(W.bits_to_f32(c.q, c.dtype).astype(np.float64))
+    k = torch.from_numpy(W.bits_to_f32(c.k, c.dtype).astype(np.float64))
+    v = torch.from_numpy(W.bits_to_f32(c.v, c.dtype).astype(np.float64))
+    for b in range(c.num_seqs):
+        q0, q1 = int(c.cu_q[b]), int(c.cu_q[b + 1])
+        k0, k1 = int(c.cu_k[b]), int(c.cu_k[b + 1])
+        qlen, klen = q1 - q0, k1 - k0
+        mask = torch.arange(klen)[None, :] <= (klen - qlen + torch.arange(qlen))[:, None]
+        ref = F.scaled_dot_product_attention(q[q0:q1].permute(1, 0, 2),
+                                             k[k0:k1].permute(1, 0, 2),
+                                             v[k0:k1].permute(1, 0, 2), attn_mask=mask,
+                                             scale=c.scale)
+        np.testing.assert_allclose(o64[q0:q1], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_varlen_sequences_are_independent_bitwise():
+    c = _varlen(seed=5, ql=(4, 7, 2), kl=(6, 7, 5))
+    o64, _ = oracle.varlen_attention(c.q, c.k, c.v, c.cu_q, c.cu_k, c.scale, c.dtype)
+    order = [2, 0, 1]
+    ql, kl = np.diff(c.cu_q), np.diff(c.cu_k)
+    qs = np.concatenate([c.q[c.cu_q[b]:c.cu_q[b + 1]] for b in order])
+    ks = np.concatenate([c.k[c.cu_k[b]:c.cu_k[b + 1]] for b in order])
+    vs = np.concatenate([c.v[c.cu_k[b]:c.cu_k[b + 1]] for b in order])
+    cq = np.concatenate([[0], np.cumsum(ql[order])]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(kl[order])]).astype(np.int32)
+    o2, _ = oracle.varlen_attention(qs, ks, vs, cq, ck, c.scale, c.dtype)
+    ref = np.concatenate([o64[c.cu_q[b]:c.cu_q[b + 1]] for b in order])
+    assert np.array_equal(o2, ref)
+
+
+def test_varlen_rejects_fewer_keys_than_queries():
+    c = _varlen(seed=6, ql=(3,), kl=(3,))
+    with pytest.raises(ValueError):
+        oracle.varlen_attention(c.q, c.k[:2], c.v[:2], c.cu_q, np.array([0, 2], np.int32),
+                                c.scale, c.dtype)

@@ -373,6 +373,79 @@ def long_context_decode(seed: int = 0, batch: int = 8, lo: int = 16384,
                      num_splits=num_splits)
 
 
+@dataclasses.dataclass
+class VarlenCase:
+    """A varlen batch with contiguous keys and values (no cache): sequence b
+    has query rows q[cu_q[b]:cu_q[b+1]] and key/value rows
+    k, v[cu_k[b]:cu_k[b+1]]."""
+    name: str
+    dtype: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    scale: float
+    q: np.ndarray        # [Tq, Hq, D] bits
+    k: np.ndarray        # [Tk, Hkv, D] bits
+    v: np.ndarray
+    cu_q: np.ndarray     # [B+1] int32
+    cu_k: np.ndarray
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.cu_q.shape[0] - 1)
+
+    @property
+    def total_query_tokens(self) -> int:
+        return int(self.cu_q[-1])
+
+    @property
+    def max_query_len(self) -> int:
+        d = np.diff(self.cu_q)
+        return int(d.max()) if d.size else 0
+
+    def flops(self) -> float:
+        """QK^T and PV, 4 * Hq * D per (query row, visible key)."""
+        ql, kl = np.diff(self.cu_q).astype(np.int64), np.diff(self.cu_k).astype(np.int64)
+        keys = ql * (kl - ql) + ql * (ql + 1) // 2
+        return 4.0 * self.num_heads * self.head_dim * float(keys.sum())
+
+
+def make_varlen_case(name: str, *, seed: int, dtype: int, num_heads: int,
+                     num_kv_heads: int, head_dim: int, q_lens, k_lens=None,
+                     scale: Optional[float] = None,
+                     rng: Optional[np.random.Generator] = None) -> VarlenCase:
+    """Seeded N(0,1) q, k, v for a varlen batch; k_lens defaults to q_lens
+    (causal self-attention over each prompt); k_lens >= q_lens."""
+    if rng is None:
+        rng = np.random.default_rng(seed)
+    ql = np.asarray(q_lens, dtype=np.int64)
+    kl = ql.copy() if k_lens is None else np.asarray(k_lens, dtype=np.int64)
+    assert kl.shape == ql.shape and np.all(kl >= ql) and np.all(ql >= 0)
+    cu_q = np.zeros(ql.size + 1, np.int32)
+    cu_q[1:] = np.cumsum(ql)
+    cu_k = np.zeros(kl.size + 1, np.int32)
+    cu_k[1:] = np.cumsum(kl)
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    q = _normal_bits(rng, (int(cu_q[-1]), num_heads, head_dim), dtype)
+    k = _normal_bits(rng, (int(cu_k[-1]), num_kv_heads, head_dim), dtype)
+    v = _normal_bits(rng, (int(cu_k[-1]), num_kv_heads, head_dim), dtype)
+    return VarlenCase(name=name, dtype=dtype, num_heads=num_heads,
+                      num_kv_heads=num_kv_heads, head_dim=head_dim, scale=float(scale),
+                      q=q, k=k, v=v, cu_q=cu_q, cu_k=cu_k)
+
+
+def varlen_prefill_llama8b(seed: int = 0, batch: int = 16, lo: int = 128,
+                           hi: int = 2048) -> VarlenCase:
+    """Prompt prefill before any cache write, Llama-3.1-8B shape (32 query /
+    8 KV heads, head_dim 128, bf16): 16 prompts of uniform [128, 2048]
+    tokens, causal self-attention over each."""
+    rng = np.random.default_rng(seed)
+    ql = rng.integers(lo, hi + 1, size=batch)
+    return make_varlen_case("varlen_prefill_llama8b", seed=seed, rng=rng, dtype=BF16,
+                            num_heads=32, num_kv_heads=8, head_dim=128, q_lens=ql)
+
+
 # Vision tokens per image of a Llama-3.2-Vision-style encoder: 1601 per
 # image tile (1600 patches and a class token), 1 to 4 tiles.  The page on
 # cross-attention QKV (vLLM PR #7448, discussion) measures that model family
