@@ -196,6 +196,38 @@ PA_API int paged_attn_cross_attention(const void* q, const void* k_cache,
                                int num_splits, void* out, void* workspace,
                                size_t workspace_bytes, pa_stream_t stream);
 
+/* Workspace size in bytes for gqa_varlen_prefill. */
+PA_API size_t gqa_varlen_prefill_workspace_bytes(int num_seqs, int total_query_tokens,
+                                                 int num_heads, int num_kv_heads,
+                                                 int head_dim);
+
+/*
+ * gqa_varlen_prefill -- prompt attention over the new tokens' own keys and
+ * values, before any cache write, without expanding K/V per query head
+ * (vLLM issue #1880, "[Performance] Use optimized kernels for MQA/GQA",
+ * item 1: the prefill path broadcasts K/V [T, Hkv, D] to [T, Hq, D] and
+ * runs a multi-head kernel; here each KV head's rows are read once for its
+ * G query heads).
+ *
+ *   q [total_query_tokens, num_heads, head_dim]; k, v
+ *   [total_key_tokens, num_kv_heads, head_dim], contiguous (device).
+ *   Sequence b owns query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key
+ *   rows [cu_seqlens_k[b], cu_seqlens_k[b+1]) (int32, device, num_seqs + 1
+ *   entries, starting at 0); its key count must be at least its query count.
+ *   Causal, bottom-right: with klen keys and qlen rows, row t sees keys
+ *   0 .. klen - qlen + t; cu_seqlens_q == cu_seqlens_k is plain causal
+ *   self-attention over each prompt.  max_seqlen_q bounds the chunk length.
+ *   out has q's shape.  Errors as for the paged entry points; a sequence
+ *   with fewer keys than query rows is skipped and flagged
+ *   PA_DEV_BAD_LENGTHS in the workspace status word.
+ */
+PA_API int gqa_varlen_prefill(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                              int total_query_tokens, int total_key_tokens,
+                              int max_seqlen_q, float scale, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_dim, int dtype, void* out,
+                              void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
 /*
  * Read (and clear, if `clear` != 0) the device status word kept in a
  * workspace after the work queued on `stream` so far has finished.  This

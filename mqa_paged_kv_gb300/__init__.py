@@ -60,6 +60,11 @@ _lib.paged_attn_chunked_prefill.argtypes = [_P, _P, _P, _P, _I, _P, _P, _I, _I, 
 _lib.paged_attn_chunked_prefill.restype = _I
 _lib.paged_attn_cross_attention.argtypes = _lib.paged_attn_chunked_prefill.argtypes
 _lib.paged_attn_cross_attention.restype = _I
+_lib.gqa_varlen_prefill_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+_lib.gqa_varlen_prefill_workspace_bytes.restype = _SZ
+_lib.gqa_varlen_prefill.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _F, _I, _I, _I, _I, _I,
+                                    _P, _P, _SZ, _P]
+_lib.gqa_varlen_prefill.restype = _I
 _lib.pa_read_device_status.argtypes = [_P, _I, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.pa_read_device_status.restype = _I
 
@@ -74,7 +79,8 @@ EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_l
             "paged_attn_workspace_bytes", "paged_attn_decode",
             "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
             "pa_read_device_status", "paged_attn_decode_noalloc",
-            "paged_attn_cross_attention"]
+            "paged_attn_cross_attention", "gqa_varlen_prefill_workspace_bytes",
+            "gqa_varlen_prefill"]
 
 
 class PagedAttnError(RuntimeError):
@@ -235,6 +241,35 @@ def paged_attn_cross_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         _dtype_code(q), num_splits, _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "paged_attn_cross_attention")
+    return out
+
+
+def gqa_varlen_prefill_workspace_bytes(num_seqs: int, total_query_tokens: int, num_heads: int,
+                                       num_kv_heads: int, head_dim: int) -> int:
+    return int(_lib.gqa_varlen_prefill_workspace_bytes(num_seqs, total_query_tokens, num_heads,
+                                                       num_kv_heads, head_dim))
+
+
+def gqa_varlen_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                       max_seqlen_q: int, scale: float, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q [Tq, Hq, D], k, v [Tk, Hkv, D] contiguous; cu_seqlens int32 [B+1]
+    -> out [Tq, Hq, D] (bottom-right causal per sequence, no cache)."""
+    _contig(q, k, v, cu_seqlens_q, cu_seqlens_k, out)
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    B = cu_seqlens_q.shape[0] - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_workspace(gqa_varlen_prefill_workspace_bytes(B, Tq, Hq, Hkv, D),
+                                    q.device)
+    rc = _lib.gqa_varlen_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), Tq, Tk, int(max_seqlen_q), float(scale), B,
+                                 Hq, Hkv, D, _dtype_code(q), _ptr(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gqa_varlen_prefill")
     return out
 
 

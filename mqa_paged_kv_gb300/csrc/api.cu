@@ -109,6 +109,24 @@ int encode_cache_map(CUtensorMap* map, const void* base, int64_t rows, int head_
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// 3-D map over contiguous K or V [T][Hkv][D]: boxes of (64 columns, one KV
+// head, 64 tokens) -- one 8 KB copy per 64 columns of a 64-key stage.
+int encode_varlen_kv_map(CUtensorMap* map, const void* base, int64_t tokens, int num_kv_heads,
+                         int head_dim) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                           static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 // 3-D map over q [T][Hq][D]: boxes of (64 columns, G heads, TQ tokens).
 int encode_query_map(CUtensorMap* map, const void* base, int64_t tokens, int num_heads,
                      int head_dim, int G, int TQ) {
@@ -170,6 +188,15 @@ WsLayout prefill_layout(int num_seqs, int total_query_tokens, int num_heads, int
                    static_cast<int64_t>(num_seqs) * (TQ - 1)) / TQ + 1;
   if (tiles > total_query_tokens) tiles = total_query_tokens;
   return workspace_layout(num_seqs, num_heads, head_dim, pairs, tiles);
+}
+
+WsLayout varlen_layout(int num_seqs, int total_query_tokens, int num_heads, int num_kv_heads,
+                       int head_dim) {
+  const int TQ = prefill_tokens_per_tile(num_heads / num_kv_heads);
+  int64_t tiles = (static_cast<int64_t>(total_query_tokens) +
+                   static_cast<int64_t>(num_seqs) * (TQ - 1)) / TQ + 1;
+  if (tiles > total_query_tokens) tiles = total_query_tokens;
+  return workspace_layout(num_seqs, num_heads, head_dim, 0, tiles);
 }
 
 int check_workspace(const void* ws, size_t bytes, const WsLayout& L) {
@@ -256,6 +283,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.total_tokens = total_query_tokens;
   pp.causal = causal;
+  pp.cu_key_lens = nullptr;
 
   PrefillParams fp;
   fp.block_tables = block_tables;
@@ -272,6 +300,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   fp.tokens_per_tile = TQ;
   fp.box_rows = box_rows;
   fp.causal = causal;
+  fp.varlen = 0;
   fp.scale_log2 = scale * 1.4426950408889634f;
 
   DecodeParams dp;
@@ -434,6 +463,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_seq = max_blocks_per_seq;
   pp.total_tokens = num_seqs;
   pp.causal = 1;
+  pp.cu_key_lens = nullptr;
 
   DecodeParams dp;
   dp.q = q;
@@ -514,6 +544,101 @@ int paged_attn_cross_attention(const void* q, const void* k_cache, const void* v
                          context_lens, total_query_tokens, max_query_len, scale, num_seqs,
                          num_heads, num_kv_heads, head_dim, block_size, num_blocks, dtype,
                          num_splits, out, workspace, workspace_bytes, stream, 0);
+}
+
+size_t gqa_varlen_prefill_workspace_bytes(int num_seqs, int total_query_tokens, int num_heads,
+                                          int num_kv_heads, int head_dim) {
+  if (num_seqs < 0 || total_query_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+      num_heads % num_kv_heads != 0 || head_dim <= 0)
+    return 0;
+  return varlen_layout(num_seqs, total_query_tokens, num_heads, num_kv_heads, head_dim).total;
+}
+
+int gqa_varlen_prefill(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_k, int total_query_tokens, int total_key_tokens,
+                       int max_seqlen_q, float scale, int num_seqs, int num_heads,
+                       int num_kv_heads, int head_dim, int dtype, void* out, void* workspace,
+                       size_t workspace_bytes, pa_stream_t stream) {
+  g_last_launches = 0;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_HEADDIM;
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+      num_heads / num_kv_heads > 64)
+    return PA_ERR_SHAPE;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (total_query_tokens < 0 || total_key_tokens < 0 || max_seqlen_q < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0 || total_query_tokens == 0) return PA_OK;
+  if (total_key_tokens <= 0) return PA_ERR_SHAPE;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return PA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PA_ERR_ALIGN;
+  const WsLayout L = varlen_layout(num_seqs, total_query_tokens, num_heads, num_kv_heads, head_dim);
+  int rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, L)) != PA_OK) return rc;
+  DeviceInfo dev;
+  if ((rc = current_device(dev)) != PA_OK) return rc;
+
+  const int G = num_heads / num_kv_heads;
+  const int TQ = prefill_tokens_per_tile(G);
+  CUtensorMap tmk, tmv, tmq;
+  if ((rc = encode_varlen_kv_map(&tmk, k, total_key_tokens, num_kv_heads, head_dim)) != PA_OK)
+    return rc;
+  if ((rc = encode_varlen_kv_map(&tmv, v, total_key_tokens, num_kv_heads, head_dim)) != PA_OK)
+    return rc;
+  if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
+      PA_OK)
+    return rc;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool bf16 = dtype == PA_BF16;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  PrepareParams pp = {};
+  pp.context_lens = nullptr;
+  pp.cu_query_lens = cu_seqlens_q;
+  pp.cu_key_lens = cu_seqlens_k;
+  pp.out = out;
+  pp.hdr = reinterpret_cast<WsHeader*>(ws);
+  pp.seq_info = reinterpret_cast<SeqInfo*>(ws + L.seq_info);
+  pp.pairs = reinterpret_cast<DecPair*>(ws + L.pairs);
+  pp.tiles = reinterpret_cast<PfTile*>(ws + L.tiles);
+  pp.num_seqs = num_seqs;
+  pp.block_size = 16;  // unused with contiguous K/V (no decode list)
+  pp.num_splits = 1;
+  pp.num_kv_heads = num_kv_heads;
+  pp.num_heads = num_heads;
+  pp.head_dim = head_dim;
+  pp.tokens_per_tile = TQ;
+  pp.max_blocks_per_seq = 0;
+  pp.total_tokens = total_query_tokens;
+  pp.causal = 1;
+  PrefillParams fp = {};
+  fp.block_tables = nullptr;
+  fp.context_lens = nullptr;
+  fp.out = out;
+  fp.tiles = pp.tiles;
+  fp.hdr = pp.hdr;
+  fp.mbs = 0;
+  fp.num_heads = num_heads;
+  fp.num_kv_heads = num_kv_heads;
+  fp.G = G;
+  fp.block_size = 16;
+  fp.num_blocks = 0;
+  fp.tokens_per_tile = TQ;
+  fp.box_rows = 64;
+  fp.causal = 1;
+  fp.varlen = 1;
+  fp.scale_log2 = scale * 1.4426950408889634f;
+
+  const ProfileScope prof(st);
+  int n = 0, r;
+  if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
+  n += r;
+  prof.begin();
+  if ((r = launch_prefill_tc(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
+                             dev.num_sms)) < 0)
+    return cuda_error();
+  n += r;
+  prof.end();
+  return finish(n);
 }
 
 int pa_read_device_status(const void* workspace, int clear, uint32_t* flags, pa_stream_t stream) {

@@ -58,7 +58,8 @@ struct PfTile {
   int32_t ntok;   // valid query tokens in the tile
   int32_t pos0;   // absolute position of the first token (ctx - qlen + i)
   int32_t nkv;    // keys the tile reads: pos0 + ntok (causal) or ctx (cross)
-  int32_t pad[3];
+  int32_t kbase;  // contiguous (varlen) K/V: row of the sequence's first key
+  int32_t pad[2];
 };
 
 struct WsLayout {
@@ -118,6 +119,8 @@ struct PrepareParams {
   int tokens_per_tile;  // prefill tile height in tokens
   int max_blocks_per_seq;
   int causal;           // 0: cross-attention, every row sees all keys, qlen may exceed ctx
+  const int32_t* cu_key_lens;  // varlen K/V (no cache): key rows of sequence b are
+                               // [cu_key_lens[b], cu_key_lens[b+1]); all rows take tiles
   int64_t total_tokens;  // rows of q / out
 };
 
@@ -154,6 +157,7 @@ struct PrefillParams {
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks, tokens_per_tile;
   int box_rows;  // keys per K/V box: gcd(block_size, 64), so a box never crosses a block
   int causal;    // 0: cross-attention (every row sees all of the tile's keys)
+  int varlen;    // 1: K/V are contiguous [T, Hkv, D] tensors (3-D maps), no block table
   float scale_log2;
 };
 

@@ -175,9 +175,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool boxer = lane < nb;
     const int my_j = lane / C::kBoxes, my_bx = lane % C::kBoxes;
     uint32_t t_iter = 0, c = 0;  // c: ring position of the next load
+    int cur_kvh = 0;             // KV head of the current item (contiguous K/V)
     bool ok = true;
 
-    // One slot: K or V of one stage, each lane its own 16-key box.
+    // One slot: K or V of one stage, each lane its own box.
     auto load_slot = [&](const CUtensorMap* map, int row) -> bool {
       const int s = static_cast<int>(c % kSlots);
       if (c >= static_cast<uint32_t>(kSlots) &&
@@ -185,7 +186,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return false;
       if (lane == 0) mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
       __syncwarp();
-      if (boxer)
+      if (boxer && p.varlen)  // 64 consecutive tokens of one KV head; row = token
+        tma_load_3d(ring + s * C::kSlot + my_bx * C::kRegion, map, my_bx * 64, cur_kvh, row,
+                    &bar[kBarSlotFull + s]);
+      else if (boxer)
         tma_load_2d(ring + s * C::kSlot + my_bx * C::kRegion + my_j * box_rows * 128, map,
                     my_bx * 64, row,
                     &bar[kBarSlotFull + s]);
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int kvh = static_cast<int>(it - ti * static_cast<uint32_t>(Hkv));
       const PfTile tile = p.tiles[ti];
       const int nkv = tile.nkv;
+      cur_kvh = kvh;
       if (lane == 0) {
         TcMeta m;
         m.tok0 = tile.tok0;
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // is loaded while the current one is in use.
       auto load_window = [&](int lblk0) -> int {
         const int lb = lblk0 + lane;
-        return (lb * bs < nkv)
+        return (!p.varlen && lb * bs < nkv)  // contiguous K/V have no block table
                    ? __ldg(p.block_tables + static_cast<int64_t>(tile.b) * p.mbs + lb)
                    : -1;
       };
@@ -272,11 +277,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
 
       // K(0), then K(j), V(j - 1) for j = 1 .. n - 1, then V(n - 1): the
-      // order the MMAs consume them in.
+      // order the MMAs consume them in.  Contiguous K/V: the stage's first
+      // token; keys past the sequence read the next sequence's rows (or
+      // zeros past the tensor), which the mask and the V-row zeroing cover.
       const int n = (nkv + kTcKeys - 1) / kTcKeys;
       int prev_row = oob_row;
       for (int j = 0; j < n && ok; ++j) {
-        const int row = stage_row(j * kTcKeys);
+        const int row = p.varlen ? tile.kbase + j * kTcKeys : stage_row(j * kTcKeys);
         ok = load_slot(&tmk, row);
         if (ok && j >= 1) ok = load_slot(&tmv, prev_row);
         prev_row = row;

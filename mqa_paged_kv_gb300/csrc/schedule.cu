@@ -21,16 +21,21 @@ constexpr int kDecBuckets = 128;  // by 16-key stages, clamped
 constexpr int kPfBuckets = 256;   // by 64-key stages, clamped
 
 struct SeqPlan {
-  int qlen, ctx, tok;
+  int qlen, ctx, tok, kbase;
   int nsplit, chunk_keys;  // decode
   int ntile;               // prefill
   bool bad;                // lengths outside the contract: no work, flagged
 };
 
 __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
-  SeqPlan s{0, 0, 0, 0, 0, 0, false};
+  SeqPlan s{0, 0, 0, 0, 0, 0, 0, false};
   if (b >= p.num_seqs) return s;
-  s.ctx = p.context_lens[b];
+  if (p.cu_key_lens) {  // contiguous K/V of a varlen batch
+    s.kbase = p.cu_key_lens[b];
+    s.ctx = p.cu_key_lens[b + 1] - s.kbase;
+  } else {
+    s.ctx = p.context_lens[b];
+  }
   if (p.cu_query_lens) {
     s.tok = p.cu_query_lens[b];
     s.qlen = p.cu_query_lens[b + 1] - s.tok;
@@ -39,15 +44,15 @@ __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
     s.qlen = 1;
   }
   const int ctx = s.ctx;
-  const int max_ctx = p.max_blocks_per_seq * p.block_size;
-  if (ctx < 0 || ctx > max_ctx || s.qlen < 0 || (p.causal && s.qlen > ctx && ctx > 0) || s.tok < 0 ||
+  const int max_ctx = p.cu_key_lens ? ctx : p.max_blocks_per_seq * p.block_size;
+  if (ctx < 0 || ctx > max_ctx || s.kbase < 0 || s.qlen < 0 || (p.causal && s.qlen > ctx && ctx > 0) || s.tok < 0 ||
       static_cast<int64_t>(s.tok) + s.qlen > p.total_tokens) {
     s.bad = true;
     s.qlen = 0;
     return s;
   }
   if (ctx == 0) return s;  // no key: the query rows are zero (written below)
-  if (s.qlen == 1) {
+  if (s.qlen == 1 && !p.cu_key_lens) {
     const int nb = (ctx + p.block_size - 1) / p.block_size;
     int chunk;
     if (p.num_splits > 0) {
@@ -59,7 +64,7 @@ __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
     }
     s.nsplit = (nb + chunk - 1) / chunk;
     s.chunk_keys = chunk * p.block_size;
-  } else if (s.qlen > 1) {
+  } else if (s.qlen >= 1) {  // chunks; with contiguous K/V every row
     s.ntile = (s.qlen + p.tokens_per_tile - 1) / p.tokens_per_tile;
   }
   return s;
@@ -228,7 +233,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
       tl.ntok = min(s.qlen - t * p.tokens_per_tile, p.tokens_per_tile);
       tl.pos0 = s.ctx - s.qlen + t * p.tokens_per_tile;
       tl.nkv = p.causal ? tl.pos0 + tl.ntok : s.ctx;
-      tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
+      tl.kbase = s.kbase;
+      tl.pad[0] = tl.pad[1] = 0;
       const int pos = atomicAdd(&pf_cnt[pf_bucket(tl.nkv)], 1);
       p.tiles[pos] = tl;
     }

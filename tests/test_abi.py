@@ -120,3 +120,21 @@ def test_last_cuda_error_starts_clear(lib):
     # Host-side validation failures are not CUDA errors and leave it clear.
     assert lib._lib.pa_last_cuda_error() == 0
     assert lib._lib.pa_last_cuda_error_string() == b"no error"
+
+
+def test_varlen_prefill_rejects_bad_arguments(lib):
+    f = lib._lib.gqa_varlen_prefill
+    P = ctypes.c_void_p
+    good = dict(Tq=64, Tk=64, maxq=64, scale=0.1, B=1, Hq=32, Hkv=8, D=128, dtype=1)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(P(16), P(16), P(16), P(16), P(16), a["Tq"], a["Tk"], a["maxq"], a["scale"],
+                 a["B"], a["Hq"], a["Hkv"], a["D"], a["dtype"], P(16), P(256), 1 << 20, None)
+    assert call(dtype=7) == -3          # PA_ERR_DTYPE
+    assert call(D=96) == -4             # PA_ERR_HEADDIM
+    assert call(Hkv=5) == -2            # Hq % Hkv
+    assert call(scale=0.0) == -2        # scale must be > 0
+    assert call(Tk=0) == -2             # keys needed when there are query rows
+    assert call(B=0) == 0 and call(Tq=0) == 0   # nothing to do
+    assert lib.gqa_varlen_prefill_workspace_bytes(16, 4096, 32, 8, 128) > 0

@@ -323,3 +323,49 @@ def test_cross_attention_prefill_workload_sampled_rows():
     rows = np.random.default_rng(0).choice(c.total_query_tokens, size=48, replace=False)
     rows.sort()
     run_and_check(c, rows=rows)
+
+
+# --------------------------------------------------------------------------
+# GQA prefill over contiguous varlen K/V (no cache, no expansion)
+# --------------------------------------------------------------------------
+
+def _run_varlen(c, rows=None):
+    import mqa_paged_kv_gb300 as pa
+    from gpu_harness import elem_dtype, to_dev
+    et = elem_dtype(c)
+    q, k, v = to_dev(c.q, et), to_dev(c.k, et), to_dev(c.v, et)
+    cq, ck = to_dev(c.cu_q), to_dev(c.cu_k)
+    out = torch.full_like(q, float("nan"))
+    ws = pa.alloc_workspace(pa.gqa_varlen_prefill_workspace_bytes(
+        c.num_seqs, c.total_query_tokens, c.num_heads, c.num_kv_heads, c.head_dim), q.device)
+    pa.gqa_varlen_prefill(q, k, v, cq, ck, c.max_query_len, c.scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_status(ws) == 0
+    o64, ob = oracle.varlen_attention(c.q, c.k, c.v, c.cu_q, c.cu_k, c.scale, c.dtype, rows=rows)
+    got = bits(out)
+    if rows is not None:
+        got = got[np.asarray(rows)]
+    return check_attention(got, o64, ob, c.dtype)
+
+
+@pytest.mark.parametrize("hq,hkv,D,dtype", [(32, 8, 128, W.BF16), (16, 16, 64, W.F16),
+                                            (32, 4, 128, W.F16), (32, 1, 128, W.BF16)])
+def test_varlen_prefill_prompts(hq, hkv, D, dtype):
+    # prompt lengths around the 64-key stage and the tile heights, incl. 1
+    ql = np.array([1, 63, 64, 65, 200, 513, 7])
+    c = W.make_varlen_case("varlen", seed=hq * 3 + hkv + D, dtype=dtype, num_heads=hq,
+                           num_kv_heads=hkv, head_dim=D, q_lens=ql)
+    _run_varlen(c)
+
+
+def test_varlen_prefill_chunks_after_a_prefix():
+    # more keys than query rows: the chunk sits at the end (bottom-right)
+    c = W.make_varlen_case("varlen_prefix", seed=77, dtype=W.BF16, num_heads=32, num_kv_heads=8,
+                           head_dim=128, q_lens=[40, 1, 130, 64], k_lens=[300, 90, 131, 64])
+    _run_varlen(c)
+
+
+def test_varlen_prefill_workload_sampled_rows():
+    c = W.varlen_prefill_llama8b(0)
+    rows = np.sort(np.random.default_rng(1).choice(c.total_query_tokens, 48, replace=False))
+    _run_varlen(c, rows=rows)
