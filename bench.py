@@ -438,6 +438,57 @@ def prefill_roofline(workload: str, seed: int, device, args, flush):
             "timed_on": f"the {pcase.num_seqs} query chunks of {workload} (seed {seed}) alone"}
 
 
+def measure_varlen(seed: int, device, steps: int, warmup: int, flush):
+    """gqa_varlen_prefill on the Llama-3.1-8B prompt batch (16 prompts of
+    U[128, 2048] tokens, contiguous K/V, no cache): CUDA-event time of the
+    whole call and of its prefill kernel, tensor roofline of the kernel."""
+    import torch
+    import mqa_paged_kv_gb300 as pa
+    c = W.varlen_prefill_llama8b(seed)
+    et = torch.bfloat16
+
+    def dev(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(dt)
+        return t.to(device)
+    q, k, v = dev(c.q, et), dev(c.k, et), dev(c.v, et)
+    cq, ck = dev(c.cu_q), dev(c.cu_k)
+    out = torch.empty_like(q)
+    ws = pa.alloc_workspace(pa.gqa_varlen_prefill_workspace_bytes(
+        c.num_seqs, c.total_query_tokens, c.num_heads, c.num_kv_heads, c.head_dim), device)
+
+    def call(prof=None):
+        if prof is not None:
+            pa.pa_profile_next_call(*prof)
+        pa.gqa_varlen_prefill(q, k, v, cq, ck, c.max_query_len, c.scale, out=out, workspace=ws)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in ev:
+        flush.sum()
+        e[0].record(stream)
+        call()
+        e[1].record(stream)
+    for e in ev:
+        flush.sum()
+        call((e[2], e[3]))
+    torch.cuda.synchronize()
+    t = float(np.mean([e[0].elapsed_time(e[1]) for e in ev])) / 1e3
+    kt = float(np.mean([e[2].elapsed_time(e[3]) for e in ev])) / 1e3
+    flops = c.flops()
+    peak, src = measured_bf16_peak()
+    ach = flops / kt / 1e12
+    return {"tokens_per_s": c.total_query_tokens / t, "ms_per_step": t * 1e3,
+            "query_tokens": c.total_query_tokens,
+            "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": ach,
+                         "peak": peak, "peak_source": src, "unit": "TFLOP/s",
+                         "frac": ach / peak, "kernel_ms": kt * 1e3, "algorithmic_flops": flops,
+                         "traffic": None}}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -536,6 +587,8 @@ def run_ours(args):
             "kv_gbs": mcase.kv_bytes() / ms / 1e9, "query_tokens": mcase.total_query_tokens,
             "roofline": prefill_roofline("mixed_prefill_decode", args.seed + rank, device,
                                          args, flush)}}
+        line["secondary"]["varlen_prefill_llama8b"] = measure_varlen(
+            args.seed + rank, device, max(5, args.steps // 2), 3, flush)
 
     if rank == 0 and not args.no_cpu_baseline:
         try:

@@ -112,7 +112,7 @@ __device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity
 
 // Eleven warps put three on three of the SM's four register files, which
 // caps a thread at 168 registers; a softmax thread's 128 scores fit in that.
-template <bool kBF16, int D>
+template <bool kBF16, int D, bool kVarlen>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv,
@@ -186,13 +186,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return false;
       if (lane == 0) mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
       __syncwarp();
-      if (boxer && p.varlen)  // 64 consecutive tokens of one KV head; row = token
-        tma_load_3d(ring + s * C::kSlot + my_bx * C::kRegion, map, my_bx * 64, cur_kvh, row,
-                    &bar[kBarSlotFull + s]);
-      else if (boxer)
+      if constexpr (kVarlen) {  // 64 consecutive tokens of one KV head; row = token
+        if (boxer)
+          tma_load_3d(ring + s * C::kSlot + my_bx * C::kRegion, map, my_bx * 64, cur_kvh, row,
+                      &bar[kBarSlotFull + s]);
+      } else if (boxer) {
         tma_load_2d(ring + s * C::kSlot + my_bx * C::kRegion + my_j * box_rows * 128, map,
-                    my_bx * 64, row,
-                    &bar[kBarSlotFull + s]);
+                    my_bx * 64, row, &bar[kBarSlotFull + s]);
+      }
       ++c;
       return true;
     };
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // is loaded while the current one is in use.
       auto load_window = [&](int lblk0) -> int {
         const int lb = lblk0 + lane;
-        return (!p.varlen && lb * bs < nkv)  // contiguous K/V have no block table
+        return (!kVarlen && lb * bs < nkv)  // contiguous K/V have no block table
                    ? __ldg(p.block_tables + static_cast<int64_t>(tile.b) * p.mbs + lb)
                    : -1;
       };
@@ -283,7 +284,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int n = (nkv + kTcKeys - 1) / kTcKeys;
       int prev_row = oob_row;
       for (int j = 0; j < n && ok; ++j) {
-        const int row = p.varlen ? tile.kbase + j * kTcKeys : stage_row(j * kTcKeys);
+        int row;
+        if constexpr (kVarlen)
+          row = tile.kbase + j * kTcKeys;
+        else
+          row = stage_row(j * kTcKeys);
         ok = load_slot(&tmk, row);
         if (ok && j >= 1) ok = load_slot(&tmv, prev_row);
         prev_row = row;
@@ -557,13 +562,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 namespace {
 
-template <bool kBF16, int D>
+template <bool kBF16, int D, bool kVarlen>
 int launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                         const PrefillParams& p, int64_t max_items, cudaStream_t stream,
                         int num_sms) {
   using C = TcCfg<D>;
   static_assert(C::kBytes <= 227 * 1024, "one CTA per SM");
-  auto kern = prefill_tc_kernel<kBF16, D>;
+  auto kern = prefill_tc_kernel<kBF16, D, kVarlen>;
   static int configured = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -594,13 +599,16 @@ int launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const CU
 int launch_prefill_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                       const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
                       cudaStream_t stream, int num_sms) {
-  if (bf16)
-    return head_dim == 64
-               ? launch_prefill_tc_t<true, 64>(tmk, tmv, tmq, p, max_items, stream, num_sms)
-               : launch_prefill_tc_t<true, 128>(tmk, tmv, tmq, p, max_items, stream, num_sms);
-  return head_dim == 64
-             ? launch_prefill_tc_t<false, 64>(tmk, tmv, tmq, p, max_items, stream, num_sms)
-             : launch_prefill_tc_t<false, 128>(tmk, tmv, tmq, p, max_items, stream, num_sms);
+#define PA_PREFILL_LAUNCH(B, DIM, V) \
+  launch_prefill_tc_t<B, DIM, V>(tmk, tmv, tmq, p, max_items, stream, num_sms)
+  const bool v = p.varlen != 0;
+  if (bf16) {
+    if (head_dim == 64) return v ? PA_PREFILL_LAUNCH(true, 64, true) : PA_PREFILL_LAUNCH(true, 64, false);
+    return v ? PA_PREFILL_LAUNCH(true, 128, true) : PA_PREFILL_LAUNCH(true, 128, false);
+  }
+  if (head_dim == 64) return v ? PA_PREFILL_LAUNCH(false, 64, true) : PA_PREFILL_LAUNCH(false, 64, false);
+  return v ? PA_PREFILL_LAUNCH(false, 128, true) : PA_PREFILL_LAUNCH(false, 128, false);
+#undef PA_PREFILL_LAUNCH
 }
 
 }  // namespace pa
