@@ -13,16 +13,16 @@
 // stage gathered from the cache feeds 256 rows.
 //
 // Warp roles (one CTA per SM, persistent over a device tile list):
-//   warp 0     TMA producer: the two Q tiles (one 3-D box per 64 columns
-//              each), then K and V of the visible keys in 64-key stages
-//              through one ring of slots, in the order the MMAs consume
-//              them (K0, K1, V0, K2, V1, ...); a slot is boxes of
-//              gcd(block_size, 64) keys gathered through the block table,
-//              one box per lane, issued by one instruction;
+//   warps 0, 3 TMA producers (0: the item records, the two Q tiles -- one
+//              3-D box per 64 columns each -- and K; 3: V): the visible
+//              keys in 64-key stages through one ring of slots, in the
+//              order the MMAs consume them (K0, K1, V0, K2, V1, ...); a slot
+//              is boxes of gcd(block_size, 64) keys gathered through the
+//              block table, one box per lane, issued by one instruction;
 //   warps 1-2  MMA issuers, one per tile: S_t = Q_t K^T (M 128, N 64)
 //              into one of two S buffers in tensor memory, O_t += P_t V
 //              with P_t read from tensor memory (O in tensor memory);
-//   warps 3-10 softmax, four warps per tile, one thread per row (= TMEM
+//   warps 4-11 softmax, four warps per tile, one thread per row (= TMEM
 //              lane): scale, bottom-right causal mask, running max,
 //              P = 2^(x*scale - m) in the element type written over the
 //              first half of its own S buffer in tensor memory, fp32 row
@@ -44,12 +44,16 @@ constexpr int kTcRows = 128;              // M of one tile
 constexpr int kTcKeys = 64;               // keys per stage: N of QK, K of PV
 constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per slot; PV K-steps
 constexpr int kTcSoftmaxWarps = 8;
-constexpr int kTcFirstSoftmaxWarp = 3;  // warp 0 producer, warps 1-2 MMA issuers
+// warp 0 the K producer, warps 1-2 the MMA issuers, warp 3 the V producer;
+// with the softmax warps after them every SM sub-partition (warp % 4) holds
+// one of these four and one softmax warp of each tile.
+constexpr int kTcVProducerWarp = 3;
+constexpr int kTcFirstSoftmaxWarp = 4;
 constexpr int kTcThreads = (kTcFirstSoftmaxWarp + kTcSoftmaxWarps) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 of the largest unnormalised P
 
 struct TcMeta {
-  int32_t tok0, ntok, pos0, kvh, nkv, done, b, pad;
+  int32_t tok0, ntok, pos0, kvh, nkv, done, b, kbase;
 };
 
 enum : int {
@@ -110,8 +114,8 @@ __device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity
 
 }  // namespace
 
-// Eleven warps put three on three of the SM's four register files, which
-// caps a thread at 168 registers; a softmax thread's 128 scores fit in that.
+// Twelve warps put three on each of the SM's four register files, which
+// caps a thread at 168 registers.
 template <bool kBF16, int D, bool kVarlen>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar[kBarQFull], 1);
-    mbar_init(&bar[kBarQEmpty], 2 + kTcSoftmaxWarps);  // two MMA commits + meta reads
+    mbar_init(&bar[kBarQEmpty], 3 + kTcSoftmaxWarps);  // two MMA commits + meta reads
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
       mbar_init(&bar[kBarPFull + i], 4);
@@ -159,13 +163,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* status = &p.hdr->status;
   const uint32_t num_items = p.hdr->prefill_items;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == 0 || warp == kTcVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    // Two warps issue the K/V copies (measured on this part: L2-resident
+    // 2 KB boxes arrive about 1.5x faster from two issuing warps than from
+    // one).  The K warp grabs the work items, publishes each item's record
+    // and loads its Q tiles; the V warp reads the record once Q has landed.
+    // Each fills its own positions of the one ring, whose order
+    // K0, K1, V0, K2, V1, ... is the MMAs' consumption order.
+    const bool is_v = warp == kTcVProducerWarp;
+    if (lane == 0 && !is_v) {
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       tma_prefetch_desc(&tmq);
     }
+    const CUtensorMap* map = is_v ? &tmv : &tmk;
     const int oob_row = p.num_blocks * Hkv * bs;  // a box here reads zeros
     // A slot is 64 / box_rows boxes of box_rows keys per 64 columns; box j
     // of column half bx belongs to lane j * kBoxes + bx.
@@ -174,15 +186,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nb = kboxes * C::kBoxes;             // boxes per slot (<= 8)
     const bool boxer = lane < nb;
     const int my_j = lane / C::kBoxes, my_bx = lane % C::kBoxes;
-    uint32_t t_iter = 0, c = 0;  // c: ring position of the next load
-    int cur_kvh = 0;             // KV head of the current item (contiguous K/V)
+    uint32_t t_iter = 0, c0 = 0;  // c0: ring position of the item's first load
+    int cur_kvh = 0;              // KV head of the current item (contiguous K/V)
+    // Lane i < kSlots remembers the position of this warp's i-th newest
+    // load (for the final drain); -1 = none.
+    int my_pos = -1;
     bool ok = true;
 
-    // One slot: K or V of one stage, each lane its own box.
-    auto load_slot = [&](const CUtensorMap* map, int row) -> bool {
-      const int s = static_cast<int>(c % kSlots);
-      if (c >= static_cast<uint32_t>(kSlots) &&
-          !warp_wait_or_flag(&bar[C::kBarSlotEmpty + s], ((c / kSlots) - 1) & 1, status))
+    // Ring position q: K or V of one stage, each lane its own box.
+    auto load_slot = [&](uint32_t q, int row) -> bool {
+      const int s = static_cast<int>(q % kSlots);
+      if (q >= static_cast<uint32_t>(kSlots) &&
+          !warp_wait_or_flag(&bar[C::kBarSlotEmpty + s], ((q / kSlots) - 1) & 1, status))
         return false;
       if (lane == 0) mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
       __syncwarp();
@@ -194,55 +209,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_2d(ring + s * C::kSlot + my_bx * C::kRegion + my_j * box_rows * 128, map,
                     my_bx * 64, row, &bar[kBarSlotFull + s]);
       }
-      ++c;
+      const int prev = __shfl_up_sync(0xffffffffu, my_pos, 1);
+      my_pos = lane == 0 ? static_cast<int>(q) : prev;
       return true;
     };
 
     while (ok) {
-      uint32_t it = 0;
-      if (lane == 0) it = atomicAdd(&p.hdr->prefill_grab, 1u);
-      it = __shfl_sync(0xffffffffu, it, 0);
-      if (t_iter > 0 && !warp_wait_or_flag(&bar[kBarQEmpty], (t_iter - 1) & 1, status)) break;
-      if (it >= num_items) {
-        if (lane == 0) {
-          meta->done = 1;
-          mbar_arrive(&bar[kBarQFull]);
+      int tb, kvh, nkv, kbase;
+      if (!is_v) {
+        uint32_t it = 0;
+        if (lane == 0) it = atomicAdd(&p.hdr->prefill_grab, 1u);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        if (t_iter > 0 && !warp_wait_or_flag(&bar[kBarQEmpty], (t_iter - 1) & 1, status)) break;
+        if (it >= num_items) {
+          if (lane == 0) {
+            meta->done = 1;
+            mbar_arrive(&bar[kBarQFull]);
+          }
+          break;
         }
-        break;
-      }
-      const uint32_t ti = it / static_cast<uint32_t>(Hkv);
-      const int kvh = static_cast<int>(it - ti * static_cast<uint32_t>(Hkv));
-      const PfTile tile = p.tiles[ti];
-      const int nkv = tile.nkv;
-      cur_kvh = kvh;
-      if (lane == 0) {
-        TcMeta m;
-        m.tok0 = tile.tok0;
-        m.ntok = tile.ntok;
-        m.pos0 = tile.pos0;
-        m.kvh = kvh;
-        m.nkv = nkv;
-        m.done = 0;
-        m.b = tile.b;
-        m.pad = 0;
-        *meta = m;
-        mbar_arrive_expect_tx(&bar[kBarQFull],
-                              static_cast<uint32_t>(2 * C::kBoxes * 128 * G * TQ));
+        const uint32_t ti = it / static_cast<uint32_t>(Hkv);
+        kvh = static_cast<int>(it - ti * static_cast<uint32_t>(Hkv));
+        const PfTile tile = p.tiles[ti];
+        tb = tile.b;
+        nkv = tile.nkv;
+        kbase = tile.kbase;
+        if (lane == 0) {
+          TcMeta m;
+          m.tok0 = tile.tok0;
+          m.ntok = tile.ntok;
+          m.pos0 = tile.pos0;
+          m.kvh = kvh;
+          m.nkv = nkv;
+          m.done = 0;
+          m.b = tile.b;
+          m.kbase = tile.kbase;
+          *meta = m;
+          mbar_arrive_expect_tx(&bar[kBarQFull],
+                                static_cast<uint32_t>(2 * C::kBoxes * 128 * G * TQ));
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(sq + t * C::kQ + bx * C::kQRegion, &tmq, bx * 64, kvh * G,
-                        tile.tok0 + t * TQ, &bar[kBarQFull]);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_3d(sq + t * C::kQ + bx * C::kQRegion, &tmq, bx * 64, kvh * G,
+                          tile.tok0 + t * TQ, &bar[kBarQFull]);
+        }
+      } else {
+        if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
+        const TcMeta m = *meta;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kBarQEmpty]);
+        if (m.done) break;
+        tb = m.b;
+        kvh = m.kvh;
+        nkv = m.nkv;
+        kbase = m.kbase;
       }
       ++t_iter;
+      cur_kvh = kvh;
 
       // Physical block ids, 32 per window held one per lane; the next window
       // is loaded while the current one is in use.
       auto load_window = [&](int lblk0) -> int {
         const int lb = lblk0 + lane;
         return (!kVarlen && lb * bs < nkv)  // contiguous K/V have no block table
-                   ? __ldg(p.block_tables + static_cast<int64_t>(tile.b) * p.mbs + lb)
+                   ? __ldg(p.block_tables + static_cast<int64_t>(tb) * p.mbs + lb)
                    : -1;
       };
       int ids_base = 0;
@@ -263,7 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           int blk = __shfl_sync(0xffffffffu, ids, (lblk - ids_base) & 31);
           if (key < nkv && (blk < 0 || blk >= p.num_blocks)) {
-            if (lane == 0) Status::raise(status, PA_DEV_BAD_BLOCK_ID);
+            if (lane == 0 && !is_v) Status::raise(status, PA_DEV_BAD_BLOCK_ID);
             blk = -1;
           }
           const int row = (key < nkv && blk >= 0) ? (blk * Hkv + kvh) * bs + off : oob_row;
@@ -277,29 +308,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return my_row;
       };
 
-      // K(0), then K(j), V(j - 1) for j = 1 .. n - 1, then V(n - 1): the
-      // order the MMAs consume them in.  Contiguous K/V: the stage's first
-      // token; keys past the sequence read the next sequence's rows (or
-      // zeros past the tensor), which the mask and the V-row zeroing cover.
+      // Contiguous K/V: the stage's first token; keys past the sequence
+      // read the next sequence's rows (or zeros past the tensor), which the
+      // mask and the V-row zeroing cover.
       const int n = (nkv + kTcKeys - 1) / kTcKeys;
-      int prev_row = oob_row;
       for (int j = 0; j < n && ok; ++j) {
         int row;
         if constexpr (kVarlen)
-          row = tile.kbase + j * kTcKeys;
+          row = kbase + j * kTcKeys;
         else
           row = stage_row(j * kTcKeys);
-        ok = load_slot(&tmk, row);
-        if (ok && j >= 1) ok = load_slot(&tmv, prev_row);
-        prev_row = row;
+        ok = load_slot(c0 + (is_v ? vpos(j, n) : kpos(j)), row);
       }
-      if (ok) ok = load_slot(&tmv, prev_row);
+      c0 += 2 * n;
     }
     // Leave no copy in flight (the consumers may have stopped early on a
-    // timeout): wait, bounded, for the newest load of every slot.
-    for (uint32_t q = c > static_cast<uint32_t>(kSlots) ? c - kSlots : 0u; q < c; ++q)
-      if (!warp_wait_or_flag(&bar[kBarSlotFull + q % kSlots], (q / kSlots) & 1, status)) break;
-  } else if (warp < kTcFirstSoftmaxWarp) {
+    // timeout): wait, bounded, for this warp's loads among the ring's last
+    // kSlots positions, one per lane (an older position's slot has been
+    // refilled since, so its load completed and its barrier moved on).
+    const bool mine = lane < kSlots && my_pos >= 0 &&
+                      static_cast<uint32_t>(my_pos) + kSlots >= c0;
+    const uint32_t q = static_cast<uint32_t>(my_pos);
+    if (mine && !mbar_wait(&bar[kBarSlotFull + q % kSlots], (q / kSlots) & 1))
+      Status::raise(status, PA_DEV_WAIT_TIMEOUT);
+    __syncwarp();
+  } else if (warp < kTcVProducerWarp) {
     // ------------------------------------------------------------ MMA issuers
     // One warp per Q tile, so each tile's chain advances on its own while
     // the pipe runs the other tile's groups.  Per tile the QK of stage j + 1
