@@ -489,6 +489,95 @@ def measure_varlen(seed: int, device, steps: int, warmup: int, flush):
                          "traffic": None}}
 
 
+def measure_two_kernel(seed: int, device, steps: int, warmup: int, flush, block_size: int = 16):
+    """The mixed batch two ways, attention only, cache already written:
+    (a) the fused call (one work list, prefill and decode kernels back to
+    back on one stream); (b) the arrangement of vLLM PR #14431's op: a
+    prefill call over the query chunks only and a decode call over the
+    decode rows on a second stream, concurrently, with the SMs split between
+    them (pa_limit_next_call_ctas); every split in `splits` is timed."""
+    import torch
+    import mqa_paged_kv_gb300 as pa
+    c = W.mixed_prefill_decode(seed, block_size=block_size)
+    et = torch.bfloat16
+
+    def dev(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16).view(dt)
+        return t.to(device)
+    kc, vc = dev(c.k_cache, et), dev(c.v_cache, et)
+    pa.reshape_and_cache(dev(c.k_new, et), dev(c.v_new, et), kc, vc, dev(c.slot_mapping))
+    q_all = dev(c.q, et)
+    cu = np.asarray(c.cu_query_lens)
+    ql = np.diff(cu)
+    pre, dec = np.where(ql > 1)[0], np.where(ql == 1)[0]
+    rows_p = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in pre])
+    q_p, q_d = dev(c.q[rows_p], et), dev(c.q[cu[dec]], et)
+    cu_p = np.zeros(len(pre) + 1, np.int32)
+    cu_p[1:] = np.cumsum(ql[pre])
+    bt, ctx = np.asarray(c.block_tables), np.asarray(c.context_lens)
+    t_all = {"bt": dev(bt), "ctx": dev(ctx), "cu": dev(cu.astype(np.int32))}
+    t_p = {"bt": dev(bt[pre]), "ctx": dev(ctx[pre]), "cu": dev(cu_p)}
+    t_d = {"bt": dev(bt[dec]), "ctx": dev(ctx[dec])}
+    o_all, o_p, o_d = torch.empty_like(q_all), torch.empty_like(q_p), torch.empty_like(q_d)
+    H, Hkv, D, mbs = c.num_heads, c.num_kv_heads, c.head_dim, c.max_blocks_per_seq
+    ws_all = pa.alloc_workspace(pa.paged_attn_chunked_prefill_workspace_bytes(
+        c.num_seqs, c.total_query_tokens, H, Hkv, D, mbs, c.block_size, 0), device)
+    ws_p = pa.alloc_workspace(pa.paged_attn_chunked_prefill_workspace_bytes(
+        len(pre), len(rows_p), H, Hkv, D, mbs, c.block_size, 0), device)
+    ws_d = pa.alloc_workspace(pa.paged_attn_workspace_bytes(
+        len(dec), H, Hkv, D, mbs, c.block_size, 0), device)
+    main = torch.cuda.current_stream()
+    s1, s2 = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+
+    def fused():
+        pa.paged_attn_chunked_prefill(q_all, kc, vc, t_all["bt"], t_all["cu"], t_all["ctx"],
+                                      c.max_query_len, c.scale, out=o_all, workspace=ws_all)
+
+    def two(k):
+        fork = torch.cuda.Event()
+        fork.record(main)
+        s1.wait_event(fork)
+        s2.wait_event(fork)
+        pa.pa_limit_next_call_ctas(sms - k if k else 0)
+        pa.paged_attn_chunked_prefill(q_p, kc, vc, t_p["bt"], t_p["cu"], t_p["ctx"],
+                                      c.max_query_len, c.scale, out=o_p, workspace=ws_p,
+                                      stream=s1)
+        pa.pa_limit_next_call_ctas(k)
+        pa.paged_attn_decode(q_d, kc, vc, t_d["bt"], t_d["ctx"], c.scale, out=o_d,
+                             workspace=ws_d, stream=s2)
+        j1, j2 = torch.cuda.Event(), torch.cuda.Event()
+        j1.record(s1)
+        j2.record(s2)
+        main.wait_event(j1)
+        main.wait_event(j2)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(steps):
+            flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            fn()
+            b.record(main)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in ev]))
+    res = {"fused_ms": timed(fused), "two_kernel_ms": {}}
+    for k in (0, 24, 40, 56, 72):
+        res["two_kernel_ms"][str(k) if k else "no split"] = timed(lambda: two(k))
+    best = min(res["two_kernel_ms"], key=res["two_kernel_ms"].get)
+    res["best_two_kernel"] = {"decode_sms": best, "ms": res["two_kernel_ms"][best]}
+    res["note"] = ("attention only (cache written beforehand), median over steps; decode_sms = "
+                   "SMs given to the decode call, the prefill call gets the rest")
+    return res
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -587,6 +676,8 @@ def run_ours(args):
             "kv_gbs": mcase.kv_bytes() / ms / 1e9, "query_tokens": mcase.total_query_tokens,
             "roofline": prefill_roofline("mixed_prefill_decode", args.seed + rank, device,
                                          args, flush)}}
+        line["secondary"]["mixed_prefill_decode"]["two_kernel_comparison"] = measure_two_kernel(
+            args.seed + rank, device, max(5, args.steps // 2), 3, flush, args.block_size)
         line["secondary"]["varlen_prefill_llama8b"] = measure_varlen(
             args.seed + rank, device, max(5, args.steps // 2), 3, flush)
 

@@ -284,6 +284,18 @@ PA_API int paged_attn_decode_noalloc(const void* q, const void* k_cache,
  */
 PA_API void pa_profile_next_call(void* start_event, void* stop_event);
 
+/*
+ * Caps the number of CTAs (one per SM) of the persistent attention kernels
+ * of the next attention call made on this host thread (decode, chunked
+ * prefill, cross-attention or varlen prefill), so that two calls on two
+ * streams can run side by side on disjoint SMs; max_ctas <= 0 clears it.
+ * The cap is consumed by that call.  The pages define no such call: it
+ * exists to compare one fused mixed-batch launch with a prefill call and a
+ * concurrent decode call, the two-kernel arrangement of vLLM PR #14431's
+ * op (review thread on chunked_prefill_paged_decode.py).
+ */
+PA_API void pa_limit_next_call_ctas(int max_ctas);
+
 /* Library version and the number of kernels the last call enqueued. */
 PA_API int pa_version(void);
 PA_API int pa_last_launch_count(void);

@@ -42,6 +42,8 @@ _lib.pa_version.argtypes = []
 _lib.pa_version.restype = _I
 _lib.pa_last_launch_count.argtypes = []
 _lib.pa_last_launch_count.restype = _I
+_lib.pa_limit_next_call_ctas.argtypes = [_I]
+_lib.pa_limit_next_call_ctas.restype = None
 _lib.pa_last_cuda_error.argtypes = []
 _lib.pa_last_cuda_error.restype = _I
 _lib.pa_last_cuda_error_string.argtypes = []
@@ -75,7 +77,8 @@ _lib.pa_profile_next_call.argtypes = [_P, _P]
 _lib.pa_profile_next_call.restype = None
 
 EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_launch_count",
-            "pa_last_cuda_error", "pa_last_cuda_error_string", "reshape_and_cache",
+            "pa_last_cuda_error", "pa_last_cuda_error_string", "pa_limit_next_call_ctas",
+            "reshape_and_cache",
             "paged_attn_workspace_bytes", "paged_attn_decode",
             "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
             "pa_read_device_status", "paged_attn_decode_noalloc",
@@ -279,6 +282,12 @@ def pa_read_device_status(workspace: torch.Tensor, clear: bool = False, stream=N
                                     _stream(stream))
     _check(rc, "pa_read_device_status")
     return int(flags.value)
+
+
+def pa_limit_next_call_ctas(max_ctas: int) -> None:
+    """Run the next attention call's persistent kernels on at most max_ctas
+    SMs (see include/paged_attn.h)."""
+    _lib.pa_limit_next_call_ctas(int(max_ctas))
 
 
 def pa_profile_next_call(start_event, stop_event) -> None:

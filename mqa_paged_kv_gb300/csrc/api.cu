@@ -34,6 +34,7 @@ int cuda_error() {
   if (e != cudaSuccess) g_last_cuda_error = static_cast<int>(e);
   return PA_ERR_CUDA;
 }
+thread_local int g_next_ctas = 0;
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 
@@ -51,6 +52,18 @@ struct ProfileScope {
     if (stop) cudaEventRecord(stop, st);
   }
 };
+
+// The CTA cap of pa_limit_next_call_ctas, taken by the next attention call:
+// its persistent kernels run on at most that many SMs.
+int take_cta_limit() {
+  const int n = g_next_ctas;
+  g_next_ctas = 0;
+  return n;
+}
+
+int grid_sms(const DeviceInfo& dev, int limit) {
+  return (limit > 0 && limit < dev.num_sms) ? limit : dev.num_sms;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -229,6 +242,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
                 void* out, void* workspace, size_t workspace_bytes,
                 pa_stream_t stream, int causal) {
   g_last_launches = 0;
+  const int cta_limit = take_cta_limit();
   int rc = check_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                         scale, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                         num_blocks, dtype, num_splits, out);
@@ -328,11 +342,12 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   prof.begin();
   if (max_query_len > 1) {
     if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
-                dev.num_sms)) < 0)
+                grid_sms(dev, cta_limit))) < 0)
       return cuda_error();
     n += r;
   }
-  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return cuda_error();
+  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, grid_sms(dev, cta_limit))) < 0)
+    return cuda_error();
   n += r;
   prof.end();
   if (num_splits != 1) {
@@ -383,6 +398,8 @@ const char* pa_last_cuda_error_string(void) {
 
 int pa_last_launch_count(void) { return g_last_launches; }
 
+void pa_limit_next_call_ctas(int max_ctas) { g_next_ctas = max_ctas > 0 ? max_ctas : 0; }
+
 void pa_profile_next_call(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);
@@ -425,6 +442,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       int num_splits, void* out, void* workspace, size_t workspace_bytes,
                       pa_stream_t stream) {
   g_last_launches = 0;
+  const int cta_limit = take_cta_limit();
   int rc = check_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                         scale, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                         num_blocks, dtype, num_splits, out);
@@ -488,7 +506,8 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
   n += r;
   prof.begin();
-  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, dev.num_sms)) < 0) return cuda_error();
+  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, grid_sms(dev, cta_limit))) < 0)
+    return cuda_error();
   n += r;
   prof.end();
   if (num_splits != 1) {
@@ -560,6 +579,7 @@ int gqa_varlen_prefill(const void* q, const void* k, const void* v, const int32_
                        int num_kv_heads, int head_dim, int dtype, void* out, void* workspace,
                        size_t workspace_bytes, pa_stream_t stream) {
   g_last_launches = 0;
+  const int cta_limit = take_cta_limit();
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_HEADDIM;
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
@@ -634,7 +654,7 @@ int gqa_varlen_prefill(const void* q, const void* k, const void* v, const int32_
   n += r;
   prof.begin();
   if ((r = launch_prefill_tc(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
-                             dev.num_sms)) < 0)
+                             grid_sms(dev, cta_limit))) < 0)
     return cuda_error();
   n += r;
   prof.end();

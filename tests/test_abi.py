@@ -138,3 +138,9 @@ def test_varlen_prefill_rejects_bad_arguments(lib):
     assert call(Tk=0) == -2             # keys needed when there are query rows
     assert call(B=0) == 0 and call(Tq=0) == 0   # nothing to do
     assert lib.gqa_varlen_prefill_workspace_bytes(16, 4096, 32, 8, 128) > 0
+
+
+def test_cta_limit_is_a_host_setting(lib):
+    # no device call: the cap is only stored for the next attention call
+    lib.pa_limit_next_call_ctas(32)
+    lib.pa_limit_next_call_ctas(0)
