@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar[kBarQFull], 1);
-    mbar_init(&bar[kBarQEmpty], 3 + kTcSoftmaxWarps);  // two MMA commits + meta reads
+    // the softmax warps after their item's last S, the V producer after the
+    // item record
+    mbar_init(&bar[kBarQEmpty], 1 + kTcSoftmaxWarps);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
       mbar_init(&bar[kBarPFull + i], 4);
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bar[kBarSlotFull + i], 1);
-      mbar_init(&bar[C::kBarSlotEmpty + i], 2);  // one commit per tile's MMA warp
+      mbar_init(&bar[C::kBarSlotEmpty + i], 2);  // one arrival per tile
     }
     fence_mbar_init();
   }
@@ -357,19 +359,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t dv = sdesc_sw128(smem_u32(ring), C::kRegion, 1024);     // MN-major
     const uint32_t dout = tmem + C::col_o(t);
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
+    int vslot[2] = {0, 0};  // V slot read by the last PV on each S buffer
     bool ok = true;
 
     // S_t(j) = Q_t K(j)^T once K(j) landed and the PV two stages back no
-    // longer reads that S buffer.
+    // longer reads that S buffer -- nor its V slot, which this warp then
+    // releases (a plain arrival: a second tcgen05.commit right behind
+    // another one costs the issuing warp about 250 cycles on this part).
     auto issue_qk = [&](int j, int n) -> bool {
       const uint32_t g = g0 + j;
       const int b = static_cast<int>(g & 1);
       const uint32_t ck = c0 + kpos(j);
       const int sk = static_cast<int>(ck % kSlots);
-      if (!warp_wait_or_flag(&bar[kBarSlotFull + sk], (ck / kSlots) & 1, status) ||
-          (g >= 2 &&
-           !warp_wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status)))
-        return false;
+      if (!warp_wait_or_flag(&bar[kBarSlotFull + sk], (ck / kSlots) & 1, status)) return false;
+      if (g >= 2) {
+        if (!warp_wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status))
+          return false;
+        if (lane == 0) mbar_arrive(&bar[C::kBarSlotEmpty + (b ? vslot[1] : vslot[0])]);
+      }
       tc_fence_after();
       const uint64_t dks = dk + static_cast<uint64_t>((sk * C::kSlot) >> 4);
       const uint32_t ds = tmem + C::col_s(t, b);
@@ -379,8 +386,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       dks + (((ks >> 2) * C::kRegion + (ks & 3) * 32) >> 4), kIdQK,
                       ks > 0 ? 1u : 0u);
       umma_commit_warp(&bar[kBarSFull + 2 * t + b]);
-      umma_commit_warp(&bar[C::kBarSlotEmpty + sk]);
-      if (j == n - 1) umma_commit_warp(&bar[kBarQEmpty]);
       return true;
     };
     // O_t += P_t(j) V(j) once V(j) landed, P_t(j) is written and (first
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int ks = 1; ks < kTcSub; ++ks)
         umma_f16_ts_warp(dout, ap + ks * 8, dvs + ((ks * 2048) >> 4), kIdPV, 1u);
       umma_commit_warp(&bar[kBarPvDone + 2 * t + b]);
-      umma_commit_warp(&bar[C::kBarSlotEmpty + sv]);
+      if (b) vslot[1] = sv; else vslot[0] = sv;
       if (j == n - 1) umma_commit_warp(&bar[kBarOFull + t]);
       return true;
     };
@@ -440,7 +445,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TcMeta m = *meta;
       __syncwarp();
       if (m.done) break;
-      if (lane == 0) mbar_arrive(&bar[kBarQEmpty]);
       const int tl = t * TQ + row / G;  // token within the pair
       const bool valid = row < rows_used && tl < m.ntok;
       // causal: the row's absolute position; cross-attention: every key
@@ -455,6 +459,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = false;
           break;
         }
+        // S_t(j) complete: this tile's QK no longer reads K(j) (one warp per
+        // tile releases its slot) and, after the item's last stage, Q.
+        if (lane == 0 && quarter == 0)
+          mbar_arrive(&bar[C::kBarSlotEmpty + (c0 + kpos(j)) % kSlots]);
+        if (lane == 0 && j == n - 1) mbar_arrive(&bar[kBarQEmpty]);
         tc_fence_after();
         float x[kTcKeys];
         tmem_ld64f(lane_base + C::col_s(t, b), x);
