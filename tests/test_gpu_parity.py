@@ -382,3 +382,40 @@ def test_cta_limit_gives_the_same_bits():
     out = g.attention()
     torch.cuda.synchronize()
     assert np.array_equal(bits(out), ref)
+
+
+# --------------------------------------------------------------------------
+# large sizes: batches beyond one work-list pass, long single chunks
+# --------------------------------------------------------------------------
+
+def test_decode_batch_beyond_one_work_list_pass():
+    # more sequences than the work-list kernel's 512 threads: the multi-pass
+    # path (split offsets read back from the workspace)
+    c = W.llama8b_decode(31, batch=1500, max_ctx=1024)
+    rows = np.sort(np.random.default_rng(3).choice(c.num_seqs, 96, replace=False))
+    run_and_check(c, rows=rows)
+
+
+def test_mixed_batch_beyond_one_work_list_pass():
+    c = W.mixed_prefill_decode(32, n_prefill=40, n_decode=700, q_range=(2, 96),
+                               prior_range=(0, 300), dec_range=(16, 600))
+    rows = np.sort(np.random.default_rng(4).choice(c.total_query_tokens, 96, replace=False))
+    run_and_check(c, rows=rows)
+
+
+def test_one_long_chunk():
+    # 4096 query tokens of one sequence after a 1000-token prefix: 64 tile pairs
+    c = W.make_case("long_chunk", seed=33, dtype=W.BF16, num_heads=32, num_kv_heads=8,
+                    head_dim=128, block_size=16, context_lens=[5096, 40],
+                    query_lens=[4096, 1])
+    rows = np.sort(np.concatenate([np.random.default_rng(5).choice(4096, 40, replace=False),
+                                   [0, 4095, 4096]]))
+    run_and_check(c, rows=rows)
+
+
+def test_varlen_one_long_prompt():
+    c = W.make_varlen_case("varlen_long", seed=34, dtype=W.BF16, num_heads=32, num_kv_heads=8,
+                           head_dim=128, q_lens=[8192, 3])
+    rows = np.sort(np.concatenate([np.random.default_rng(6).choice(8192, 40, replace=False),
+                                   [8191, 8192, 8194]]))
+    _run_varlen(c, rows=rows)
