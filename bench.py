@@ -75,8 +75,8 @@ def make_workload(name: str, seed: int, block_size: int = 16):
                         "cross_attention_prefill"):
             raise SystemExit("--block-size applies to llama8b_decode, mixed_prefill_decode "
                              "and the cross_attention workloads")
-        return W.CONFIGS[name](seed, block_size=block_size)
-    return W.CONFIGS[name](seed)
+        return W.WORKLOADS[name](seed, block_size=block_size)
+    return W.WORKLOADS[name](seed)
 
 
 # ---------------------------------------------------------------- env helpers

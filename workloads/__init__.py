@@ -478,7 +478,7 @@ def cross_attention_prefill(seed: int = 0, batch: int = 16, q_range=(32, 512),
                            block_size=block_size, encoder_lens=enc, query_lens=ql)
 
 
-CONFIGS = {
+WORKLOADS = {
     "tiny_gqa_decode": tiny_gqa_decode,
     "llama8b_decode": llama8b_decode,
     "mixed_prefill_decode": mixed_prefill_decode,
