@@ -372,16 +372,30 @@ def time_steps(step, steps, warmup, flush, e2e=False):
     L2 is flushed before every timed step, outside the timed interval."""
     torch = step.torch
     stream = torch.cuda.current_stream()
-    host = dev_bufs = None
+    host_pack = dev_pack = dev_bufs = None
     if e2e:
-        host = {k: v.cpu().pin_memory() for k, v in step.inputs.items()}
-        dev_bufs = {k: torch.empty_like(v) for k, v in step.inputs.items()}
+        # The step's inputs travel as one pinned host buffer and one copy
+        # (tensors at 256-byte aligned offsets, device views into one buffer).
+        offs, off = {}, 0
+        for k, v in step.inputs.items():
+            offs[k] = off
+            off += (v.numel() * v.element_size() + 255) // 256 * 256
+        host_pack = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+        dev_pack = torch.empty(max(off, 256), dtype=torch.uint8, device=step.out.device)
+        dev_bufs = {}
+        for k, v in step.inputs.items():
+            nb = v.numel() * v.element_size()
+            if nb == 0:  # an empty input (no new K/V in a cross-attention step)
+                dev_bufs[k] = torch.empty_like(v)
+                continue
+            host_pack[offs[k]:offs[k] + nb].copy_(
+                v.contiguous().reshape(-1).view(torch.uint8).cpu())
+            dev_bufs[k] = dev_pack[offs[k]:offs[k] + nb].view(v.dtype).view(v.shape)
         out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
 
     def one(prof=None):
         if e2e:
-            for k in host:
-                dev_bufs[k].copy_(host[k], non_blocking=True)
+            dev_pack.copy_(host_pack, non_blocking=True)
             o = step.run(dev_bufs, prof)
             out_host.copy_(o, non_blocking=True)
         else:
