@@ -7,18 +7,31 @@
 // the kernel exploits the sharing; item 2 names the paged decode kernel).
 //
 // Structure:
-//  * persistent CTAs of 8 warps; warps form groups of ceil(G / 8) warps, and
-//    each group pulls items from a device work list with one atomic per item;
+//  * persistent CTAs; warps form groups, and each group pulls items from a
+//    device work list with one atomic per item;
 //  * per group, a ring of R stages; a stage is a 16-key tile of K and V
-//    (one TMA box per 64 columns, 128-byte swizzle) plus, for the first tile
-//    of an item, the G query rows (one bulk copy); the first warp of the
-//    group issues the copies R stages ahead, so HBM reads of the next tiles
-//    (and of the next item) overlap the math on the current one;
-//  * the grouped dot products run on tensor cores with the KV tokens on the
-//    MMA's M side ("swap AB": S^T = K Q^T, O^T += V^T P^T) so a 16-key tile
-//    fills the 16 rows and the query heads sit on the 8-wide N side;
-//    P^T is turned into the B operand of the second MMA with movmatrix;
-//  * online softmax in base 2 with fp32 running max / sum per head column;
+//    (one TMA box per 64 columns, 128-byte swizzle); the group's producer
+//    issues the copies R stages ahead, so HBM reads of the next tiles (and
+//    of the next item) overlap the math on the current one;
+//  * the grouped dot products run on tensor cores (mma.sync m16n8k16) in one
+//    of two orientations, chosen by G:
+//    - G <= 8, "swap AB": the KV tokens sit on the MMA's M side
+//      (S^T = K Q^T, O^T += V^T P^T), so a 16-key tile fills the 16 rows and
+//      the query heads sit on the 8-wide N side; one warp per group, which
+//      also issues its own copies; the G query rows travel with the first
+//      stage of an item; P^T becomes the B operand of the second MMA with
+//      movmatrix;
+//    - G > 8, "head major": each consumer warp owns 16 query heads on the M
+//      side (S = Q K^T, O += P V), so P leaves the first MMA already in the
+//      A-operand layout of the second; a group is ceil(G / 16) consumer
+//      warps plus one warp that only issues copies; the query rows of an
+//      item go to one of two slots per group, released by the consumers
+//      once they hold them in registers;
+//  * online softmax in base 2 with fp32 running max / sum per head; the
+//    head-major path moves its reference max only when a row's max grows by
+//    more than 2^8 (the exponentials stay below 2^8, which fp32 sums and the
+//    16-bit P operand carry at full relative precision), so most tiles skip
+//    the rescale of the accumulators;
 //  * items that cover a whole sequence write the output row; split items
 //    write an fp32 partial and its log-sum-exp, merged by combine_kernel,
 //    which is launched as a programmatic dependent of this kernel so that
@@ -30,27 +43,36 @@ namespace pa {
 namespace {
 
 struct StageMeta {
-  int32_t tok, kvh, key_base, nvalid, part_idx, flags, b, pad;
+  int32_t tok, kvh, key_base, nvalid, part_idx, flags, b, qslot;
 };
 constexpr int kFirst = 1, kLast = 2, kDone = 4;
 
-template <int D, int GS>
+// Head-major path: the reference max moves only when a row's max exceeds it
+// by more than this many powers of two.
+constexpr float kRefSlack = 8.f;
+
+template <int D, int GS, bool kHM>
 struct DecodeTile {
-  static constexpr int kBoxes = D / 64;       // 64-column TMA boxes per row
-  static constexpr int kKV = kBoxes * 2048;   // one 16-key tile of K (or V)
-  static constexpr int kQ = GS * 8 * D * 2;   // query rows of one group
-  static constexpr int kStage = 2 * kKV + kQ;
-  static_assert(kStage % 1024 == 0, "stages keep 1024-byte alignment");
+  static constexpr int kBoxes = D / 64;        // 64-column TMA boxes per row
+  static constexpr int kKV = kBoxes * 2048;    // one 16-key tile of K (or V)
+  static constexpr int kRows = kHM ? 16 : 8;   // query heads per consumer warp
+  static constexpr int kQ = GS * kRows * D * 2;  // query rows of one group
+  // swap AB keeps the query rows in every stage, head major in two slots
+  static constexpr int kStage = kHM ? 2 * kKV : 2 * kKV + kQ;
+  static_assert(kStage % 1024 == 0 && kQ % 1024 == 0, "1024-byte alignment");
 };
 
-template <int D, int GS, int NW, int R>
+template <int D, int GS, int NW, int R, bool kHM>
 struct DecodeSmem {
-  using T = DecodeTile<D, GS>;
-  static constexpr int kGroups = NW / GS;
+  using T = DecodeTile<D, GS, kHM>;
+  static constexpr int kWarpsPerGroup = kHM ? GS + 1 : GS;
+  static constexpr int kGroups = NW / kWarpsPerGroup;
   static constexpr int kRing = kGroups * R * T::kStage;
-  static constexpr int kBars = kGroups * R * 2 * 8;
+  static constexpr int kQSlots = kHM ? kGroups * 2 * T::kQ : 0;
+  static constexpr int kBarsPerGroup = 2 * R + (kHM ? 2 : 0);  // full, empty, query slots
+  static constexpr int kBars = kGroups * kBarsPerGroup * 8;
   static constexpr int kMeta = kGroups * R * static_cast<int>(sizeof(StageMeta));
-  static constexpr int kBytes = kRing + kBars + kMeta + 1024;  // + alignment slack
+  static constexpr int kBytes = kRing + kQSlots + kBars + kMeta + 1024;  // + alignment slack
 };
 
 // Producer-side description of the item whose tiles are being issued.
@@ -71,37 +93,52 @@ struct Next {
 
 }  // namespace
 
-template <bool kBF16, int D, int GS, int NW, int R>
+template <bool kBF16, int D, int GS, int NW, int R, bool kHM>
 __global__ void __launch_bounds__(NW * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
-  using T = DecodeTile<D, GS>;
-  using S = DecodeSmem<D, GS, NW, R>;
-  constexpr int kMT = D / 16;  // 16-row MMA tiles along D
+  using T = DecodeTile<D, GS, kHM>;
+  using S = DecodeSmem<D, GS, NW, R, kHM>;
+  constexpr int kMT = D / 16;  // 16-wide MMA steps along D
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int group = warp / GS, wig = warp % GS;
+  const int group = warp / S::kWarpsPerGroup, wig = warp % S::kWarpsPerGroup;
   uint8_t* ring = smem + group * R * T::kStage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kRing) + group * 2 * R;
+  uint8_t* qslots = smem + S::kRing + group * 2 * T::kQ;  // head major only
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>(smem + S::kRing + S::kQSlots) + group * S::kBarsPerGroup;
   uint64_t* empty = full + R;
-  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + S::kRing + S::kBars) + group * R;
+  uint64_t* qempty = full + 2 * R;  // head major only
+  StageMeta* meta =
+      reinterpret_cast<StageMeta*>(smem + S::kRing + S::kQSlots + S::kBars) + group * R;
 
   // Query slots start zeroed: rows past G are never written and feed the
-  // padded N columns of the MMA.
-  for (int i = threadIdx.x; i < S::kGroups * R * (T::kQ / 16); i += blockDim.x) {
-    const int st = i / (T::kQ / 16), c = i % (T::kQ / 16);
-    reinterpret_cast<uint4*>(smem + st * T::kStage + 2 * T::kKV)[c] = make_uint4(0, 0, 0, 0);
+  // padded rows (head major) or N columns (swap AB) of the MMA.
+  if constexpr (kHM) {
+    for (int i = threadIdx.x; i < S::kQSlots / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(smem + S::kRing)[i] = make_uint4(0, 0, 0, 0);
+  } else {
+    for (int i = threadIdx.x; i < S::kGroups * R * (T::kQ / 16); i += blockDim.x) {
+      const int st = i / (T::kQ / 16), c = i % (T::kQ / 16);
+      reinterpret_cast<uint4*>(smem + st * T::kStage + 2 * T::kKV)[c] = make_uint4(0, 0, 0, 0);
+    }
   }
   if (threadIdx.x == 0) {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing);
-    for (int g = 0; g < S::kGroups; ++g)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRing + S::kQSlots);
+    for (int g = 0; g < S::kGroups; ++g) {
+      uint64_t* gb = bars + g * S::kBarsPerGroup;
       for (int s = 0; s < R; ++s) {
-        mbar_init(bars + g * 2 * R + s, 1);
-        mbar_init(bars + g * 2 * R + R + s, GS);
+        mbar_init(gb + s, 1);
+        mbar_init(gb + R + s, GS);
       }
+      if (kHM) {
+        mbar_init(gb + 2 * R, GS);
+        mbar_init(gb + 2 * R + 1, GS);
+      }
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
@@ -113,12 +150,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   const uint32_t num_items = p.hdr->decode_items;
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
-  const bool producer = (wig == 0);
+  const bool producer = kHM ? (wig == GS) : (wig == 0);
   uint32_t* status = &p.hdr->status;
   const uint16_t* qg = static_cast<const uint16_t*>(p.q);
 
   // ---------------------------------------------------------------- producer
   uint32_t p_iter = 0;
+  uint32_t q_items = 0;  // items whose query rows were issued (head major)
   bool p_finished = false;
   Cursor cur;
   cur.key = cur.key_end = 0;
@@ -169,7 +207,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   auto issue_stage = [&]() {
     if (p_finished) return;
     const int s = static_cast<int>(p_iter % R);
-    if (GS > 1 && p_iter >= static_cast<uint32_t>(R)) {
+    // A swap-AB group of one warp consumes its own copies in order and never
+    // runs more than R stages ahead of itself.
+    if ((kHM || GS > 1) && p_iter >= static_cast<uint32_t>(R)) {
       if (!mbar_wait_warp(&empty[s], ((p_iter / R) - 1) & 1)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         p_finished = true;
@@ -215,6 +255,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const int y = (blk * Hkv + cur.kvh) * bs + (key_base - lblk * bs);
     const bool first = cur.first;
     const bool last = key_base + kKeyTile >= cur.key_end;
+    int qslot = 0;
+    if (kHM && first) {
+      // The slot's previous item must be held in the consumers' registers.
+      qslot = static_cast<int>(q_items & 1);
+      if (q_items >= 2 && !mbar_wait_warp(&qempty[qslot], ((q_items >> 1) - 1) & 1)) {
+        if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
+        p_finished = true;
+        return;
+      }
+      ++q_items;
+    }
     if (lane == 0) {
       StageMeta m;
       m.tok = cur.tok;
@@ -224,7 +275,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       m.part_idx = cur.part;
       m.flags = (first ? kFirst : 0) | (last ? kLast : 0);
       m.b = cur.b;
-      m.pad = 0;
+      m.qslot = qslot;
       meta[s] = m;
       const uint32_t qbytes = first ? static_cast<uint32_t>(G * D * 2) : 0u;
       mbar_arrive_expect_tx(&full[s], 2 * T::kKV + qbytes);
@@ -237,7 +288,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if (first) {
         const uint16_t* src =
             qg + (static_cast<int64_t>(cur.tok) * Hq + static_cast<int64_t>(cur.kvh) * G) * D;
-        bulk_load(st + 2 * T::kKV, src, qbytes, &full[s]);
+        bulk_load(kHM ? qslots + qslot * T::kQ : st + 2 * T::kKV, src, qbytes, &full[s]);
       }
     }
     cur.key += kKeyTile;
@@ -246,190 +297,378 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (nx.state < 3) advance();
   };
 
-  // ---------------------------------------------------------------- consumer
-  const int g = lane >> 2, q4 = lane & 3;
-  const int mi = lane >> 3, rr = lane & 7;
-  float acc[kMT][4];
-  float mrow[2], lrow[2];
-  uint32_t qf[kMT][2];
-#pragma unroll
-  for (int i = 0; i < kMT; ++i) {
-    acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    qf[i][0] = qf[i][1] = 0u;
-  }
-  mrow[0] = mrow[1] = -INFINITY;
-  lrow[0] = lrow[1] = 0.f;
+  const int g = lane >> 2, q4 = lane & 3;   // MMA fragment: row group, column pair
+  const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix index, row in it
 
-  auto finalize = [&](const StageMeta& m) {
-    float l0 = lrow[0], l1 = lrow[1];
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  if constexpr (kHM) {
+    // ------------------------------------------------ head major, G > 8
+    if (producer) {
+      while (!p_finished) issue_stage();
+      // Leave no copy in flight: wait (bounded) for the latest fill of each
+      // slot, so the CTA never exits with TMA writes pending.
+      for (uint32_t i = p_iter > static_cast<uint32_t>(R) ? p_iter - R : 0u; i < p_iter; ++i)
+        if (!mbar_wait_warp(&full[i % R], (i / R) & 1)) break;
+      return;
     }
-    const float il0 = l0 > 0.f ? 1.f / l0 : 0.f;
-    const float il1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    const int hb = 8 * wig;
-    if (m.part_idx < 0) {
-      uint16_t* out = static_cast<uint16_t*>(p.out) +
-                      (static_cast<int64_t>(m.tok) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
-      const int h = hb + g;
+    constexpr int kNT = D / 8;  // 8-column output tiles along D
+    float o[kNT][4];
+    uint32_t qa[kMT][4];
+    float mref[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};  // rows g, g + 8
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-        const uint32_t t0 =
-            movmatrix_t(pack2<kBF16>(acc[mt][0] * il0, acc[mt][1] * il1));
-        const uint32_t t1 =
-            movmatrix_t(pack2<kBF16>(acc[mt][2] * il0, acc[mt][3] * il1));
-        if (h < G) {
-          uint32_t* o = reinterpret_cast<uint32_t*>(out + h * D + mt * 16 + 2 * q4);
-          o[0] = t0;
-          o[4] = t1;  // +8 elements
-        }
-      }
-    } else {
-      float* po = p.part_o +
-                  (static_cast<int64_t>(m.part_idx) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
-      const int h0 = hb + 2 * q4, h1 = h0 + 1;
+    for (int i = 0; i < kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-        const int d0 = mt * 16 + g, d1 = d0 + 8;
-        if (h0 < G) {
-          po[h0 * D + d0] = acc[mt][0] * il0;
-          po[h0 * D + d1] = acc[mt][2] * il0;
-        }
-        if (h1 < G) {
-          po[h1 * D + d0] = acc[mt][1] * il1;
-          po[h1 * D + d1] = acc[mt][3] * il1;
-        }
-      }
-      if (g == 0) {
-        float* pl = p.part_lse + static_cast<int64_t>(m.part_idx) * Hq +
-                    static_cast<int64_t>(m.kvh) * G;
-        if (h0 < G) pl[h0] = l0 > 0.f ? mrow[0] + __log2f(l0) : -INFINITY;
-        if (h1 < G) pl[h1] = l1 > 0.f ? mrow[1] + __log2f(l1) : -INFINITY;
-      }
-    }
-  };
+    for (int i = 0; i < kMT; ++i) qa[i][0] = qa[i][1] = qa[i][2] = qa[i][3] = 0u;
+    const int h0 = 16 * wig + g, h1 = h0 + 8;  // this lane's two heads
 
-  if (producer)
-    for (int i = 0; i < R; ++i) issue_stage();
-
-  uint32_t c_iter = 0;
-  while (true) {
-    const int s = static_cast<int>(c_iter % R);
-    if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
-      if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
-      break;
-    }
-    const StageMeta m = meta[s];
-    if (m.flags & kDone) break;
-    const uint32_t kbase = smem_u32(ring + s * T::kStage);
-    const uint32_t vbase = kbase + T::kKV;
-    const uint32_t qbase = kbase + 2 * T::kKV;
-
-    if (m.flags & kFirst) {
-#pragma unroll
-      for (int i = 0; i < kMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-      mrow[0] = mrow[1] = -INFINITY;
-      lrow[0] = lrow[1] = 0.f;
-      // B operand (Q^T): rows = this warp's 8 heads, 16-byte chunks along D.
-#pragma unroll
-      for (int ks = 0; ks < kMT; ks += 2) {
-        const int row = 8 * wig + rr;
-        const int chunk = 2 * ks + mi;
-        uint32_t r[4];
-        ldsm_x4(qbase + row * (D * 2) + chunk * 16, r);
-        qf[ks][0] = r[0];
-        qf[ks][1] = r[1];
-        qf[ks + 1][0] = r[2];
-        qf[ks + 1][1] = r[3];
-      }
-    }
-
-    // S^T[16 keys][8 heads] = K Q^T, two accumulation chains.
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < kMT; ++ks) {
-      const int key = rr + ((mi & 1) << 3);
-      const int chunk = ((ks & 3) << 1) + (mi >> 1);
-      uint32_t a[4];
-      ldsm_x4(kbase + (ks >> 2) * 2048 + swz128(key, chunk), a);
-      if (ks & 1)
-        mma_16816<kBF16>(sb, a, qf[ks][0], qf[ks][1]);
-      else
-        mma_16816<kBF16>(sa, a, qf[ks][0], qf[ks][1]);
-    }
-    float x[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = (sa[i] + sb[i]) * p.scale_log2;
-    const int nv = m.nvalid;
-    if (nv < kKeyTile) {
-      if (g >= nv) x[0] = x[1] = -INFINITY;
-      if (g + 8 >= nv) x[2] = x[3] = -INFINITY;
-    }
-
-    // Online softmax per head column (this lane: heads 2*q4, 2*q4 + 1).
-    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(mrow[0], mx0), mn1 = fmaxf(mrow[1], mx1);
-    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = ex2(mrow[0] - ref0), al1 = ex2(mrow[1] - ref1);
-    mrow[0] = mn0;
-    mrow[1] = mn1;
-    const uint32_t ptop = pack2<kBF16>(ex2(x[0] - ref0), ex2(x[1] - ref1));
-    const uint32_t pbot = pack2<kBF16>(ex2(x[2] - ref0), ex2(x[3] - ref1));
-    float p00, p01, p10, p11;
-    unpack2<kBF16>(ptop, p00, p01);
-    unpack2<kBF16>(pbot, p10, p11);
-    lrow[0] = lrow[0] * al0 + (p00 + p10);
-    lrow[1] = lrow[1] * al1 + (p01 + p11);
-    const uint32_t b0 = movmatrix_t(ptop);  // P^T rows: keys 2*q4.., column: head g
-    const uint32_t b1 = movmatrix_t(pbot);  // keys 8 + 2*q4..
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
-    }
-
-    // O^T[D][8 heads] += V^T P^T.
-    const uint32_t vm_lo = keep_mask(2 * q4 < nv, 2 * q4 + 1 < nv);
-    const uint32_t vm_hi = keep_mask(8 + 2 * q4 < nv, 9 + 2 * q4 < nv);
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt) {
-      const int key = rr + ((mi >> 1) << 3);
-      const int chunk = ((mt & 3) << 1) + (mi & 1);
-      uint32_t a[4];
-      ldsm_x4_t(vbase + (mt >> 2) * 2048 + swz128(key, chunk), a);
-      if (nv < kKeyTile) {
-        a[0] &= vm_lo;
-        a[1] &= vm_lo;
-        a[2] &= vm_hi;
-        a[3] &= vm_hi;
-      }
-      mma_16816<kBF16>(acc[mt], a, b0, b1);
-    }
-
-    __syncwarp();
-    if (GS > 1 && lane == 0) mbar_arrive(&empty[s]);
-    if (producer) issue_stage();
-    if (m.flags & kLast) finalize(m);
-    ++c_iter;
-  }
-
-  // Leave no copy in flight: wait (bounded) for stages this group issued but
-  // did not consume, so the CTA never exits with TMA writes pending.
-  if (producer) {
-    while (c_iter < p_iter) {
+    uint32_t c_iter = 0;
+    while (true) {
       const int s = static_cast<int>(c_iter % R);
-      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) break;
+      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
+        if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      const StageMeta m = meta[s];
+      if (m.flags & kDone) break;
+      const uint32_t kbase = smem_u32(ring + s * T::kStage);
+      const uint32_t vbase = kbase + T::kKV;
+
+      if (m.flags & kFirst) {
+#pragma unroll
+        for (int i = 0; i < kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        mref[0] = mref[1] = -INFINITY;
+        lsum[0] = lsum[1] = 0.f;
+        // A operand (Q): this warp's 16 heads, 16-byte chunks along D.
+        const uint32_t qbase = smem_u32(qslots + m.qslot * T::kQ) + wig * 16 * (D * 2);
+#pragma unroll
+        for (int ks = 0; ks < kMT; ++ks)
+          ldsm_x4(qbase + (rr + ((mi & 1) << 3)) * (D * 2) + (2 * ks + (mi >> 1)) * 16, qa[ks]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[m.qslot]);
+      }
+
+      // S[16 heads][16 keys] = Q K^T: keys 0-7 and 8-15 as two 8-wide N
+      // tiles, even and odd D steps on separate accumulation chains.
+      float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sa1[4] = {0.f, 0.f, 0.f, 0.f};
+      float sb0[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < kMT; ++ks) {
+        uint32_t b[4];  // keys 0-7 (low, high D half), keys 8-15 (low, high)
+        ldsm_x4(kbase + (ks >> 2) * 2048 + swz128(rr + ((mi >> 1) << 3), ((ks & 3) << 1) + (mi & 1)),
+                b);
+        if (ks & 1) {
+          mma_16816<kBF16>(sb0, qa[ks], b[0], b[1]);
+          mma_16816<kBF16>(sb1, qa[ks], b[2], b[3]);
+        } else {
+          mma_16816<kBF16>(sa0, qa[ks], b[0], b[1]);
+          mma_16816<kBF16>(sa1, qa[ks], b[2], b[3]);
+        }
+      }
+      // x[nt][0..1]: head g, keys 8nt + 2q4 (+1); x[nt][2..3]: head g + 8.
+      float x[2][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[0][i] = (sa0[i] + sb0[i]) * p.scale_log2;
+        x[1][i] = (sa1[i] + sb1[i]) * p.scale_log2;
+      }
+      const int nv = m.nvalid;
+      if (nv < kKeyTile) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int k0 = nt * 8 + 2 * q4;
+          if (k0 >= nv) x[nt][0] = x[nt][2] = -INFINITY;
+          if (k0 + 1 >= nv) x[nt][1] = x[nt][3] = -INFINITY;
+        }
+      }
+
+      // Online softmax per head row; the four lanes of a row hold 4 keys each.
+      float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const bool up0 = mx0 > mref[0] + kRefSlack, up1 = mx1 > mref[1] + kRefSlack;
+      if (__any_sync(0xffffffffu, up0 || up1)) {
+        const float al0 = up0 ? ex2(mref[0] - mx0) : 1.f;  // 0 while the row had no key
+        const float al1 = up1 ? ex2(mref[1] - mx1) : 1.f;
+        if (up0) mref[0] = mx0;
+        if (up1) mref[1] = mx1;
+        lsum[0] *= al0;
+        lsum[1] *= al1;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          o[nt][0] *= al0;
+          o[nt][1] *= al0;
+          o[nt][2] *= al1;
+          o[nt][3] *= al1;
+        }
+      }
+      const float r0 = mref[0] == -INFINITY ? 0.f : mref[0];
+      const float r1 = mref[1] == -INFINITY ? 0.f : mref[1];
+      // P in the A-operand layout of the PV MMA: a0/a1 keys 0-7, a2/a3 keys 8-15.
+      uint32_t pa[4];
+      pa[0] = pack2<kBF16>(ex2(x[0][0] - r0), ex2(x[0][1] - r0));
+      pa[1] = pack2<kBF16>(ex2(x[0][2] - r1), ex2(x[0][3] - r1));
+      pa[2] = pack2<kBF16>(ex2(x[1][0] - r0), ex2(x[1][1] - r0));
+      pa[3] = pack2<kBF16>(ex2(x[1][2] - r1), ex2(x[1][3] - r1));
+      {
+        float e0, e1, e2, e3;
+        unpack2<kBF16>(pa[0], e0, e1);
+        unpack2<kBF16>(pa[2], e2, e3);
+        lsum[0] += (e0 + e1) + (e2 + e3);
+        unpack2<kBF16>(pa[1], e0, e1);
+        unpack2<kBF16>(pa[3], e2, e3);
+        lsum[1] += (e0 + e1) + (e2 + e3);
+      }
+
+      // O[16 heads][D] += P V; V rows past the valid keys are zeroed (they
+      // may hold any bits, and 0 * NaN would reach the sum).
+      const uint32_t vm_lo = keep_mask(2 * q4 < nv, 2 * q4 + 1 < nv);
+      const uint32_t vm_hi = keep_mask(8 + 2 * q4 < nv, 9 + 2 * q4 < nv);
+#pragma unroll
+      for (int j = 0; j < kMT; ++j) {
+        uint32_t v[4];  // columns 16j..16j+7 (keys 0-7, 8-15), then 16j+8..16j+15
+        ldsm_x4_t(vbase + (j >> 2) * 2048 + swz128(rr + ((mi & 1) << 3), ((j & 3) << 1) + (mi >> 1)),
+                  v);
+        if (nv < kKeyTile) {
+          v[0] &= vm_lo;
+          v[1] &= vm_hi;
+          v[2] &= vm_lo;
+          v[3] &= vm_hi;
+        }
+        mma_16816<kBF16>(o[2 * j], pa, v[0], v[1]);
+        mma_16816<kBF16>(o[2 * j + 1], pa, v[2], v[3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+
+      if (m.flags & kLast) {
+        float l0 = lsum[0], l1 = lsum[1];
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const float il0 = l0 > 0.f ? 1.f / l0 : 0.f;
+        const float il1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        if (m.part_idx < 0) {
+          uint16_t* out = static_cast<uint16_t*>(p.out) +
+                          (static_cast<int64_t>(m.tok) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            const int d = nt * 8 + 2 * q4;
+            if (h0 < G)
+              *reinterpret_cast<uint32_t*>(out + h0 * D + d) =
+                  pack2<kBF16>(o[nt][0] * il0, o[nt][1] * il0);
+            if (h1 < G)
+              *reinterpret_cast<uint32_t*>(out + h1 * D + d) =
+                  pack2<kBF16>(o[nt][2] * il1, o[nt][3] * il1);
+          }
+        } else {
+          float* po = p.part_o +
+                      (static_cast<int64_t>(m.part_idx) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            const int d = nt * 8 + 2 * q4;
+            if (h0 < G)
+              *reinterpret_cast<float2*>(po + h0 * D + d) =
+                  make_float2(o[nt][0] * il0, o[nt][1] * il0);
+            if (h1 < G)
+              *reinterpret_cast<float2*>(po + h1 * D + d) =
+                  make_float2(o[nt][2] * il1, o[nt][3] * il1);
+          }
+          if (q4 == 0) {
+            float* pl = p.part_lse + static_cast<int64_t>(m.part_idx) * Hq +
+                        static_cast<int64_t>(m.kvh) * G;
+            if (h0 < G) pl[h0] = l0 > 0.f ? mref[0] + __log2f(l0) : -INFINITY;
+            if (h1 < G) pl[h1] = l1 > 0.f ? mref[1] + __log2f(l1) : -INFINITY;
+          }
+        }
+      }
       ++c_iter;
+    }
+  } else {
+    // ------------------------------------------------ swap AB, G <= 8
+    float acc[kMT][4];
+    float mrow[2], lrow[2];
+    uint32_t qf[kMT][2];
+#pragma unroll
+    for (int i = 0; i < kMT; ++i) {
+      acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      qf[i][0] = qf[i][1] = 0u;
+    }
+    mrow[0] = mrow[1] = -INFINITY;
+    lrow[0] = lrow[1] = 0.f;
+    auto finalize = [&](const StageMeta& m) {
+      float l0 = lrow[0], l1 = lrow[1];
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      }
+      const float il0 = l0 > 0.f ? 1.f / l0 : 0.f;
+      const float il1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      const int hb = 8 * wig;
+      if (m.part_idx < 0) {
+        uint16_t* out = static_cast<uint16_t*>(p.out) +
+                        (static_cast<int64_t>(m.tok) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+        const int h = hb + g;
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt) {
+          const uint32_t t0 =
+              movmatrix_t(pack2<kBF16>(acc[mt][0] * il0, acc[mt][1] * il1));
+          const uint32_t t1 =
+              movmatrix_t(pack2<kBF16>(acc[mt][2] * il0, acc[mt][3] * il1));
+          if (h < G) {
+            uint32_t* o = reinterpret_cast<uint32_t*>(out + h * D + mt * 16 + 2 * q4);
+            o[0] = t0;
+            o[4] = t1;  // +8 elements
+          }
+        }
+      } else {
+        float* po = p.part_o +
+                    (static_cast<int64_t>(m.part_idx) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+        const int h0 = hb + 2 * q4, h1 = h0 + 1;
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt) {
+          const int d0 = mt * 16 + g, d1 = d0 + 8;
+          if (h0 < G) {
+            po[h0 * D + d0] = acc[mt][0] * il0;
+            po[h0 * D + d1] = acc[mt][2] * il0;
+          }
+          if (h1 < G) {
+            po[h1 * D + d0] = acc[mt][1] * il1;
+            po[h1 * D + d1] = acc[mt][3] * il1;
+          }
+        }
+        if (g == 0) {
+          float* pl = p.part_lse + static_cast<int64_t>(m.part_idx) * Hq +
+                      static_cast<int64_t>(m.kvh) * G;
+          if (h0 < G) pl[h0] = l0 > 0.f ? mrow[0] + __log2f(l0) : -INFINITY;
+          if (h1 < G) pl[h1] = l1 > 0.f ? mrow[1] + __log2f(l1) : -INFINITY;
+        }
+      }
+    };
+
+    if (producer)
+      for (int i = 0; i < R; ++i) issue_stage();
+
+    uint32_t c_iter = 0;
+    while (true) {
+      const int s = static_cast<int>(c_iter % R);
+      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
+        if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
+        break;
+      }
+      const StageMeta m = meta[s];
+      if (m.flags & kDone) break;
+      const uint32_t kbase = smem_u32(ring + s * T::kStage);
+      const uint32_t vbase = kbase + T::kKV;
+      const uint32_t qbase = kbase + 2 * T::kKV;
+
+      if (m.flags & kFirst) {
+#pragma unroll
+        for (int i = 0; i < kMT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        mrow[0] = mrow[1] = -INFINITY;
+        lrow[0] = lrow[1] = 0.f;
+        // B operand (Q^T): rows = this warp's 8 heads, 16-byte chunks along D.
+#pragma unroll
+        for (int ks = 0; ks < kMT; ks += 2) {
+          const int row = 8 * wig + rr;
+          const int chunk = 2 * ks + mi;
+          uint32_t r[4];
+          ldsm_x4(qbase + row * (D * 2) + chunk * 16, r);
+          qf[ks][0] = r[0];
+          qf[ks][1] = r[1];
+          qf[ks + 1][0] = r[2];
+          qf[ks + 1][1] = r[3];
+        }
+      }
+
+      // S^T[16 keys][8 heads] = K Q^T, two accumulation chains.
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < kMT; ++ks) {
+        const int key = rr + ((mi & 1) << 3);
+        const int chunk = ((ks & 3) << 1) + (mi >> 1);
+        uint32_t a[4];
+        ldsm_x4(kbase + (ks >> 2) * 2048 + swz128(key, chunk), a);
+        if (ks & 1)
+          mma_16816<kBF16>(sb, a, qf[ks][0], qf[ks][1]);
+        else
+          mma_16816<kBF16>(sa, a, qf[ks][0], qf[ks][1]);
+      }
+      float x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = (sa[i] + sb[i]) * p.scale_log2;
+      const int nv = m.nvalid;
+      if (nv < kKeyTile) {
+        if (g >= nv) x[0] = x[1] = -INFINITY;
+        if (g + 8 >= nv) x[2] = x[3] = -INFINITY;
+      }
+
+      // Online softmax per head column (this lane: heads 2*q4, 2*q4 + 1).
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(mrow[0], mx0), mn1 = fmaxf(mrow[1], mx1);
+      const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = ex2(mrow[0] - ref0), al1 = ex2(mrow[1] - ref1);
+      mrow[0] = mn0;
+      mrow[1] = mn1;
+      const uint32_t ptop = pack2<kBF16>(ex2(x[0] - ref0), ex2(x[1] - ref1));
+      const uint32_t pbot = pack2<kBF16>(ex2(x[2] - ref0), ex2(x[3] - ref1));
+      float p00, p01, p10, p11;
+      unpack2<kBF16>(ptop, p00, p01);
+      unpack2<kBF16>(pbot, p10, p11);
+      lrow[0] = lrow[0] * al0 + (p00 + p10);
+      lrow[1] = lrow[1] * al1 + (p01 + p11);
+      const uint32_t b0 = movmatrix_t(ptop);  // P^T rows: keys 2*q4.., column: head g
+      const uint32_t b1 = movmatrix_t(pbot);  // keys 8 + 2*q4..
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+
+      // O^T[D][8 heads] += V^T P^T.
+      const uint32_t vm_lo = keep_mask(2 * q4 < nv, 2 * q4 + 1 < nv);
+      const uint32_t vm_hi = keep_mask(8 + 2 * q4 < nv, 9 + 2 * q4 < nv);
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int key = rr + ((mi >> 1) << 3);
+        const int chunk = ((mt & 3) << 1) + (mi & 1);
+        uint32_t a[4];
+        ldsm_x4_t(vbase + (mt >> 2) * 2048 + swz128(key, chunk), a);
+        if (nv < kKeyTile) {
+          a[0] &= vm_lo;
+          a[1] &= vm_lo;
+          a[2] &= vm_hi;
+          a[3] &= vm_hi;
+        }
+        mma_16816<kBF16>(acc[mt], a, b0, b1);
+      }
+
+      __syncwarp();
+      if (GS > 1 && lane == 0) mbar_arrive(&empty[s]);
+      if (producer) issue_stage();
+      if (m.flags & kLast) finalize(m);
+      ++c_iter;
+    }
+
+    // Leave no copy in flight: wait (bounded) for stages this group issued but
+    // did not consume, so the CTA never exits with TMA writes pending.
+    if (producer) {
+      while (c_iter < p_iter) {
+        const int s = static_cast<int>(c_iter % R);
+        if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) break;
+        ++c_iter;
+      }
     }
   }
 }
@@ -530,18 +769,21 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_kernel(const Combi
 // ---------------------------------------------------------------- launchers
 namespace {
 
-template <bool kBF16, int D, int GS>
+template <bool kBF16, int D, int GS, bool kHM>
 int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                     cudaStream_t stream, int num_sms) {
-  constexpr int NW = 8;
-  constexpr int kStageBytes = DecodeTile<D, GS>::kStage;
-  constexpr int kBudget = 160 * 1024;
-  constexpr int kGroups = NW / GS;
-  constexpr int kR0 = kBudget / (kGroups * kStageBytes);
+  using T = DecodeTile<D, GS, kHM>;
+  // Swap AB: 8 warps in groups of GS.  Head major: groups of GS consumer
+  // warps plus a producer warp, at most 12 warps per CTA.
+  constexpr int kGroups = kHM ? (GS == 1 ? 6 : (GS == 2 ? 4 : 8 / GS)) : 8 / GS;
+  constexpr int NW = kGroups * (kHM ? GS + 1 : GS);
+  constexpr int kBudget = (kHM ? 200 : 160) * 1024;  // ring (+ query slots) per CTA
+  constexpr int kR0 = (kBudget / kGroups - (kHM ? 2 * T::kQ : 0)) / T::kStage;
   constexpr int R = kR0 < 2 ? 2 : (kR0 > 8 ? 8 : kR0);
-  using S = DecodeSmem<D, GS, NW, R>;
+  using S = DecodeSmem<D, GS, NW, R, kHM>;
+  static_assert(S::kGroups == kGroups, "warps split into whole groups");
   static_assert(S::kBytes <= 227 * 1024, "fits one CTA per SM");
-  auto kern = decode_kernel<kBF16, D, GS, NW, R>;
+  auto kern = decode_kernel<kBF16, D, GS, NW, R, kHM>;
   static int configured = -1;  // device whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -564,14 +806,15 @@ int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
   return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, p) == cudaSuccess ? 1 : -1;
 }
 
+// G <= 8: swap AB, one warp per group.  G > 8: head major, ceil(G / 16)
+// consumer warps per group (G <= 64).
 template <bool kBF16, int D>
 int launch_decode_d(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p,
                     cudaStream_t stream, int num_sms) {
-  const int gs = (p.G + 7) / 8;
-  if (gs <= 1) return launch_decode_t<kBF16, D, 1>(tmk, tmv, p, stream, num_sms);
-  if (gs <= 2) return launch_decode_t<kBF16, D, 2>(tmk, tmv, p, stream, num_sms);
-  if (gs <= 4) return launch_decode_t<kBF16, D, 4>(tmk, tmv, p, stream, num_sms);
-  return launch_decode_t<kBF16, D, 8>(tmk, tmv, p, stream, num_sms);
+  if (p.G <= 8) return launch_decode_t<kBF16, D, 1, false>(tmk, tmv, p, stream, num_sms);
+  if (p.G <= 16) return launch_decode_t<kBF16, D, 1, true>(tmk, tmv, p, stream, num_sms);
+  if (p.G <= 32) return launch_decode_t<kBF16, D, 2, true>(tmk, tmv, p, stream, num_sms);
+  return launch_decode_t<kBF16, D, 4, true>(tmk, tmv, p, stream, num_sms);
 }
 
 }  // namespace

@@ -85,7 +85,7 @@ def test_mixed_full_size_sampled():
 
 
 # ---------------------------------------------------------------- shapes
-@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8, 12, 16, 24, 32, 48, 64])
 def test_group_sizes_decode_and_prefill(G):
     rng = np.random.default_rng(G)
     hkv = 2 if G <= 16 else 1
@@ -99,6 +99,30 @@ def test_group_sizes_decode_and_prefill(G):
                     num_kv_heads=hkv, head_dim=128, block_size=16, context_lens=ctx,
                     query_lens=np.ones(B, np.int64))
     run_and_check(d)
+
+
+@pytest.mark.parametrize("dtype,D", [(W.F16, 64), (W.BF16, 64), (W.F16, 128)])
+def test_mqa_decode_dtypes(dtype, D):
+    """Head-major decode (G > 8) in both element types and head sizes, with
+    ragged contexts that end inside a 16-key tile."""
+    rng = np.random.default_rng(41 + D)
+    ctx = np.concatenate([[1, 15, 17], rng.integers(18, 900, size=5)])
+    c = W.make_case(f"mqa_{D}", seed=41 + D, dtype=dtype, num_heads=32, num_kv_heads=1,
+                    head_dim=D, block_size=16, context_lens=ctx,
+                    query_lens=np.ones(ctx.size, np.int64))
+    run_and_check(c)
+
+
+@pytest.mark.parametrize("splits", [0, 16, 64])
+def test_mqa_long_context_outliers(splits):
+    """MQA over 16k-32k keys with 1% of the K rows scaled by 8: the head-major
+    path's reference max moves rarely and late; split partials merge."""
+    rng = np.random.default_rng(51)
+    ctx = rng.integers(16384, 32769, size=2)
+    c = W.make_case("mqa_long", seed=51, rng=rng, dtype=W.BF16, num_heads=32, num_kv_heads=1,
+                    head_dim=128, block_size=16, context_lens=ctx,
+                    query_lens=np.ones(2, np.int64), key_outlier_prob=0.01)
+    run_and_check(c, num_splits=splits)
 
 
 @pytest.mark.parametrize("bs", [32, 48, 64, 96, 128, 256])
