@@ -155,9 +155,11 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   // Pass 1: per-sequence plans, split offsets, bucket histograms.
   int carry = 0, tile_total = 0;
   int first_split_offset = 0;  // this thread's sequence in the first pass
+  SeqPlan first_plan{0, 0, 0, 0, 0, 0, 0, false};  // ... and its plan (pass 2 reuses it)
   for (int base = 0; base < p.num_seqs; base += kThreads) {
     const int b = base + tid;
     const SeqPlan s = plan_seq(p, b);
+    if (base == 0) first_plan = s;
     int excl;
     const int tot = block_scan(s.nsplit, warp_sums, excl);
     if (s.bad) Status::raise(&p.hdr->status, PA_DEV_BAD_LENGTHS);
@@ -208,7 +210,10 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   // Pass 2: emit the sorted lists and zero the rows of key-less sequences.
   for (int base = 0; base < p.num_seqs; base += kThreads) {
     const int b = base + tid;
-    const SeqPlan s = plan_seq(p, b);  // all lanes take part in the warp aggregation
+    // All lanes take part in the warp aggregation.  When one pass covers the
+    // batch the plan of pass 1 is still in registers: no second read of the
+    // lengths on the critical path.
+    const SeqPlan s = p.num_seqs <= kThreads ? first_plan : plan_seq(p, b);
     const int nfull = s.nsplit > 0 ? s.nsplit - 1 : 0;
     const int tail = s.nsplit > 0 ? s.ctx - nfull * s.chunk_keys : 0;
     const int pos_full = warp_aggregated_add(dec_cnt, dec_bucket(s.chunk_keys), nfull);
