@@ -209,6 +209,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Largest of three floats in one instruction (the three-input max of the
+// sm_100 family).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Keep the low or high 16-bit half of a pair (zero the other).
 __device__ __forceinline__ uint32_t keep_mask(bool keep_lo, bool keep_hi) {
   return (keep_lo ? 0x0000FFFFu : 0u) | (keep_hi ? 0xFFFF0000u : 0u);

@@ -475,13 +475,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int i = 0; i < kTcKeys; ++i)
             if (i > lim) x[i] = -INFINITY;
         }
+        // Row max: three-input max on eight independent chains.  (The
+        // softmax warps' instruction stream, not the tensor pipe, sets the
+        // stage time, so the row arithmetic below uses the widest forms:
+        // three-input max, and packed two-float FFMA / FADD / FMUL.)
+        static_assert(kTcKeys == 64, "the max chains cover 64 columns");
         float mx8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3f(x[e], x[e + 8], x[e + 16]);
 #pragma unroll
-        for (int i = 8; i < kTcKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3f(mx8[e], x[e + 24], x[e + 32]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3f(mx8[e], x[e + 40], x[e + 48]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], x[e + 56]);
+        const float mx = fmax3f(fmax3f(mx8[0], mx8[1], mx8[2]), fmax3f(mx8[3], mx8[4], mx8[5]),
+                                fmaxf(mx8[6], mx8[7])) *
                          p.scale_log2;
         const bool need = m_ref != -INFINITY && mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
@@ -493,12 +502,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           const float alpha = need ? ex2(m_ref - mx) : 1.f;
+          const float2 alpha2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int c = 0; c < D / 16; ++c) {
             uint32_t r[16];
             tmem_ld16(lane_base + C::col_o(t) + c * 16, r);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            for (int i = 0; i < 16; i += 2) {
+              const float2 v = __fmul2_rn(
+                  make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), alpha2);
+              r[i] = __float_as_uint(v.x);
+              r[i + 1] = __float_as_uint(v.y);
+            }
             tmem_st16(lane_base + C::col_o(t) + c * 16, r);
           }
           if (need) {
@@ -512,14 +527,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // P = 2^(x * scale - m_ref), in place, then its row sum, then the P
         // row into tensor memory over the first half of its S: column c
         // holds keys 2c, 2c+1 (those S values are already in registers).
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nr2 = make_float2(neg_ref, neg_ref);
 #pragma unroll
-        for (int i = 0; i < kTcKeys; ++i) x[i] = ex2(fmaf(x[i], p.scale_log2, neg_ref));
-        float rs8[8];
+        for (int i = 0; i < kTcKeys; i += 2) {
+          const float2 a = __ffma2_rn(make_float2(x[i], x[i + 1]), sc2, nr2);
+          x[i] = ex2(a.x);
+          x[i + 1] = ex2(a.y);
+        }
+        float2 rs[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rs8[e] = x[e];
+        for (int k = 0; k < 4; ++k) rs[k] = make_float2(x[2 * k], x[2 * k + 1]);
 #pragma unroll
-        for (int i = 8; i < kTcKeys; ++i) rs8[i & 7] += x[i];
-        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        for (int i = 8; i < kTcKeys; i += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            rs[k] = __fadd2_rn(rs[k], make_float2(x[i + 2 * k], x[i + 2 * k + 1]));
+        const float2 rsum = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+        l += rsum.x + rsum.y;
 #pragma unroll
         for (int h = 0; h < kTcKeys / 32; ++h) {
           uint32_t w[16];
