@@ -132,7 +132,6 @@ struct DecodeParams {
   float* part_lse;
   const DecPair* pairs;
   WsHeader* hdr;
-  uint32_t* done;
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks;
   float scale_log2;  // scale * log2(e)
   // 1 when the split combine follows: only then may the next launch start

@@ -113,6 +113,17 @@ def test_mqa_decode_dtypes(dtype, D):
     run_and_check(c)
 
 
+@pytest.mark.parametrize("bs", [64, 256])
+def test_mqa_decode_block_sizes(bs):
+    """Head-major decode reads its 16-key tiles through blocks of any size."""
+    rng = np.random.default_rng(61 + bs)
+    ctx = np.concatenate([[bs - 1, bs, bs + 1], rng.integers(2, 3000, size=5)])
+    c = W.make_case(f"mqa_bs{bs}", seed=61 + bs, dtype=W.BF16, num_heads=32, num_kv_heads=1,
+                    head_dim=128, block_size=bs, context_lens=ctx,
+                    query_lens=np.ones(ctx.size, np.int64))
+    run_and_check(c)
+
+
 @pytest.mark.parametrize("splits", [0, 16, 64])
 def test_mqa_long_context_outliers(splits):
     """MQA over 16k-32k keys with 1% of the K rows scaled by 8: the head-major
