@@ -87,6 +87,22 @@ def dist_env():
     return rank, world, local
 
 
+def whole_job(units: float, step_s: float, e2e_s: float, world: int, device):
+    """Whole-job figures of a replicated run (one process per GPU, each with
+    its own seeded batch): the work units of all ranks summed, and each time
+    the slowest rank's.  Collective over the default process group (NCCL on
+    GPUs; any backend works, gloo on CPU in the tests)."""
+    if world <= 1:
+        return units, step_s, e2e_s
+    import torch
+    import torch.distributed as dist
+    u = torch.tensor([units], device=device, dtype=torch.float64)
+    t = torch.tensor([step_s, e2e_s], device=device, dtype=torch.float64)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(u[0]), float(t[0]), float(t[1])
+
+
 def measured_bf16_peak():
     """Dense bf16 tensor peak (TFLOP/s) measured for a kernel timed on its own."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -624,19 +640,15 @@ def run_ours(args):
     te, _, h2d, d2h = time_steps(step, max(3, args.steps // 2), 2, flush, e2e=True)
 
     step_stats = {"min_ms": float(t.min()), "median_ms": float(np.median(t)),
-                  "max_ms": float(t.max()), "mean_ms": float(t.mean())}
-    step_s = float(t.mean()) / 1e3
+                  "p90_ms": float(np.percentile(t, 90)), "max_ms": float(t.max()),
+                  "mean_ms": float(t.mean())}
     kern_s = float(kt.mean()) / 1e3
-    e2e_s = float(te.mean()) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        v = torch.tensor([step_s, e2e_s], device=device, dtype=torch.float64)
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        step_s, e2e_s = float(v[0]), float(v[1])
-
     kvb = case.kv_bytes()
+    job_kvb, step_s, e2e_s = whole_job(float(kvb), float(t.mean()) / 1e3, float(te.mean()) / 1e3,
+                                       world, device)
+    job_tokens, _, _ = whole_job(float(case.total_query_tokens), 0.0, 0.0, world, device)
     units = "GB/s"
-    value = kvb * world / step_s / 1e9
+    value = job_kvb / step_s / 1e9
     peak, peak_src = measured_hbm_peak()
     achieved = kvb / kern_s / 1e9
     if case.is_decode:  # also cross-attention decode: the same decode kernel
@@ -669,9 +681,9 @@ def run_ours(args):
                              else "reshape_and_cache + paged attention"),
                        step_time_stats=step_stats),
         "hbm_peak_frac": value / world / peak,
-        "tokens_per_s": case.total_query_tokens * world / step_s,
+        "tokens_per_s": job_tokens / step_s,
         "roofline": roofline,
-        "e2e": {"value": kvb * world / e2e_s / 1e9, "unit": units, "ms_per_step": e2e_s * 1e3,
+        "e2e": {"value": job_kvb / e2e_s / 1e9, "unit": units, "ms_per_step": e2e_s * 1e3,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
