@@ -40,7 +40,17 @@ def _rank_main(rank, world, port, out):
         units, step_s, e2e_s = 100.0 * (rank + 1), 1e-3 * (rank + 1), 3e-3 - 1e-3 * rank
         job = bench.whole_job(units, step_s, e2e_s, w, torch.device("cpu"))
         case = bench.make_workload("tiny_gqa_decode", 7 + r)  # the bench seeds rank r with seed + r
-        out[rank] = (r, w, local, job, [int(x) for x in case.context_lens], case.num_seqs)
+        ref_ran = None
+        if rank != 0:  # the reference arm: rank 0 alone runs the oracle, the others do no work
+            import argparse
+            import contextlib
+            import io
+            buf = io.StringIO()
+            with contextlib.redirect_stdout(buf):
+                bench.run_reference(argparse.Namespace(workload="tiny_gqa_decode", seed=7,
+                                                       block_size=16, steps=1, warmup=1, gpus=2))
+            ref_ran = buf.getvalue()
+        out[rank] = (r, w, local, job, [int(x) for x in case.context_lens], case.num_seqs, ref_ran)
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -64,7 +74,7 @@ def test_two_rank_whole_job_figures():
         assert codes == [0, 0], codes
         res = dict(out)
     for rank in range(world):
-        r, w, local, job, ctx_lens, nseq = res[rank]
+        r, w, local, job, ctx_lens, nseq, _ = res[rank]
         assert (r, w, local) == (rank, world, rank)
         units, step_s, e2e_s = job
         assert units == pytest.approx(300.0)        # summed over ranks
@@ -73,6 +83,7 @@ def test_two_rank_whole_job_figures():
     # each rank has its own batch of the same shape
     assert res[0][5] == res[1][5]
     assert res[0][4] != res[1][4]
+    assert res[1][6] == ""  # a non-zero rank prints nothing for the reference arm
 
 
 def test_single_rank_passthrough():
