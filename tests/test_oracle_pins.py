@@ -216,6 +216,37 @@ def test_block_permutation_invariance_bitwise():
     assert np.array_equal(o1, o2) and np.array_equal(b1, b2)
 
 
+@pytest.mark.parametrize("bs2", [1, 2, 8, 16])
+def test_block_size_invariance_bitwise(bs2):
+    """Re-paging the same sequences into blocks of another size, under a
+    shuffled table, leaves the result bitwise unchanged: the block size only
+    decides where key j of a sequence lives (block j // bs, slot j % bs).
+    Unused slots of the new pool hold NaN, so a slot read in error shows."""
+    c = _small_case(seed=11, B=3, Hq=8, Hkv=2, D=16, bs=4,
+                    ctx=np.array([30, 17, 1]), ql=np.array([4, 1, 1]), num_blocks=20)
+    o1, b1, kc, vc = oracle.run_case(c)
+    bs = c.block_size
+    nb2 = [(int(x) + bs2 - 1) // bs2 for x in c.context_lens]
+    total = sum(nb2)
+    ids = np.random.default_rng(12).permutation(total)
+    nan_bits = np.uint16(0x7FC0)  # a bf16 quiet NaN
+    shape = (total, c.num_kv_heads, bs2, c.head_dim)
+    kc2 = np.full(shape, nan_bits, np.uint16)
+    vc2 = np.full(shape, nan_bits, np.uint16)
+    bt2 = np.full((c.num_seqs, max(nb2)), -1, np.int32)
+    k = 0
+    for b in range(c.num_seqs):
+        bt2[b, :nb2[b]] = ids[k:k + nb2[b]]
+        k += nb2[b]
+        for j in range(int(c.context_lens[b])):
+            src = c.block_tables[b, j // bs]
+            kc2[bt2[b, j // bs2], :, j % bs2] = kc[src, :, j % bs]
+            vc2[bt2[b, j // bs2], :, j % bs2] = vc[src, :, j % bs]
+    o2, b2 = oracle.paged_attention(c.q, kc2, vc2, bt2, c.cu_query_lens, c.context_lens,
+                                    c.scale, c.num_kv_heads, c.dtype)
+    assert np.array_equal(o1, o2) and np.array_equal(b1, b2)
+
+
 def test_gqa_equals_mha_with_duplicated_kv_heads_bitwise():
     c = _small_case(seed=6, B=2, Hq=8, Hkv=2, D=16, bs=4,
                     ctx=np.array([21, 9]), ql=np.array([3, 1]))
