@@ -298,6 +298,10 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   pp.total_tokens = total_query_tokens;
   pp.causal = causal;
   pp.cu_key_lens = nullptr;
+  // A batch with query chunks runs its prefill and decode kernels side by
+  // side; the work-list kernel splits the grid between them.
+  const bool concurrent = max_query_len > 1;
+  pp.split_ctas = concurrent ? grid_sms(dev, cta_limit) : 0;
 
   PrefillParams fp;
   fp.block_tables = block_tables;
@@ -315,6 +319,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   fp.box_rows = box_rows;
   fp.causal = causal;
   fp.varlen = 0;
+  fp.split_ctas = pp.split_ctas;
   fp.scale_log2 = scale * 1.4426950408889634f;
 
   DecodeParams dp;
@@ -333,14 +338,17 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   dp.num_blocks = num_blocks;
   dp.scale_log2 = fp.scale_log2;
   dp.trigger_dependents = num_splits != 1;
-
+  dp.concurrent = concurrent ? 1 : 0;
 
   const ProfileScope prof(st);
   int n = 0, r;
   if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
   n += r;
   prof.begin();
-  if (max_query_len > 1) {
+  // Prefill first: its CTAs past the prefill share leave at once, and the
+  // decode kernel, launched as its dependent, takes those SMs (and more as
+  // prefill CTAs finish).
+  if (concurrent) {
     if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
                 grid_sms(dev, cta_limit))) < 0)
       return cuda_error();
@@ -482,6 +490,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   pp.total_tokens = num_seqs;
   pp.causal = 1;
   pp.cu_key_lens = nullptr;
+  pp.split_ctas = 0;
 
   DecodeParams dp;
   dp.q = q;
@@ -499,6 +508,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   dp.num_blocks = num_blocks;
   dp.scale_log2 = scale * 1.4426950408889634f;
   dp.trigger_dependents = num_splits != 1;
+  dp.concurrent = 0;
 
 
   const ProfileScope prof(st);

@@ -145,10 +145,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
   fence_proxy_async();
   __syncthreads();
-  griddep_wait();  // the work list is written by the preceding kernel
+  // The work list is written by the work-list kernel.  Normally that is the
+  // preceding kernel and this one waits for it; beside a prefill kernel
+  // this one starts without a wait (the prefill kernel let it start only
+  // after its own wait for the list) and reads the list through L2.
+  if (!p.concurrent) griddep_wait();
   if (p.trigger_dependents) griddep_launch_dependents();  // the split combine may become resident
 
-  const uint32_t num_items = p.hdr->decode_items;
+  const uint32_t num_items = p.concurrent ? __ldcg(&p.hdr->decode_items) : p.hdr->decode_items;
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
   const bool producer = kHM ? (wig == GS) : (wig == 0);
   uint32_t* status = &p.hdr->status;
@@ -190,7 +194,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
         const uint32_t pair = it / static_cast<uint32_t>(Hkv);
         nx.kvh = static_cast<int>(it - pair * static_cast<uint32_t>(Hkv));
         const int4* rp = reinterpret_cast<const int4*>(p.pairs + pair);
-        const int4 r0 = __ldg(rp), r1 = __ldg(rp + 1);
+        const int4 r0 = p.concurrent ? __ldcg(rp) : __ldg(rp);
+        const int4 r1 = p.concurrent ? __ldcg(rp + 1) : __ldg(rp + 1);
         nx.rec.b = r0.x;
         nx.rec.tok = r0.y;
         nx.rec.key_begin = r0.z;
@@ -308,6 +313,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       // slot, so the CTA never exits with TMA writes pending.
       for (uint32_t i = p_iter > static_cast<uint32_t>(R) ? p_iter - R : 0u; i < p_iter; ++i)
         if (!mbar_wait_warp(&full[i % R], (i / R) & 1)) break;
+      if (p.concurrent) griddep_wait();  // complete after the prefill kernel beside this one
       return;
     }
     constexpr int kNT = D / 8;  // 8-column output tiles along D
@@ -671,6 +677,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     }
   }
+  if (p.concurrent) griddep_wait();  // complete after the prefill kernel beside this one
 }
 
 // Merge the split partials of each decode sequence (one CTA per sequence

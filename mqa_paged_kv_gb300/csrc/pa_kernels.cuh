@@ -28,7 +28,9 @@ struct WsHeader {
   uint32_t prefill_grab;     // next prefill item to hand out
   uint32_t prefill_items;    // prefill (tile, kv head) items
   uint32_t prefill_tiles;
-  uint32_t pad[57];
+  uint32_t decode_ctas;      // mixed batch: CTAs the decode kernel keeps (the prefill kernel
+                             // takes the SMs of the others)
+  uint32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -122,6 +124,7 @@ struct PrepareParams {
   const int32_t* cu_key_lens;  // varlen K/V (no cache): key rows of sequence b are
                                // [cu_key_lens[b], cu_key_lens[b+1]); all rows take tiles
   int64_t total_tokens;  // rows of q / out
+  int split_ctas;        // > 0: a mixed batch's grid, to be split between decode and prefill
 };
 
 struct DecodeParams {
@@ -134,9 +137,17 @@ struct DecodeParams {
   WsHeader* hdr;
   int mbs, num_heads, num_kv_heads, G, block_size, num_blocks;
   float scale_log2;  // scale * log2(e)
-  // 1 when the split combine follows: only then may the next launch start
-  // early (a following call's work-list build must not overlap this kernel).
+  // 1 when a kernel of this call follows (the split combine, or the prefill
+  // kernel of a mixed batch): only then may the next launch start early (a
+  // following call's work-list build must not overlap this kernel).
   int trigger_dependents;
+  // 1 in a batch with query chunks: launched after the prefill kernel and
+  // beside it, on the SMs its CTAs past the prefill share leave (its other
+  // CTAs join as prefill CTAs finish): no wait at the start (the work list
+  // is complete -- the prefill kernel lets this one start only after its
+  // own wait for it -- and is read through L2), and a wait for the prefill
+  // kernel before completing, so what follows sees both kernels' results.
+  int concurrent;
 };
 
 struct CombineParams {
@@ -146,6 +157,18 @@ struct CombineParams {
   void* out;
   int num_seqs, num_heads, head_dim;
 };
+
+// A batch with query chunks runs its prefill and decode kernels side by
+// side, the SMs split by the work-list kernel in proportion to the two
+// kernels' estimated times at these per-SM rates (measured on this part:
+// the decode kernel streams about 6.2 TB/s over 152 SMs, the prefill kernel
+// about 850 TFLOP/s), the decode share shaded down: decode CTAs that find
+// no SM at first take over the prefill kernel's SMs as its CTAs finish, so
+// the decode kernel can grow into a misjudged split and the prefill kernel
+// cannot.
+constexpr double kDecodeBytesPerSmSec = 41e9;
+constexpr double kPrefillFlopsPerSmSec = 5.6e12;
+constexpr double kDecodeShareMargin = 0.9;
 
 struct PrefillParams {
   const int32_t* block_tables;
@@ -157,6 +180,11 @@ struct PrefillParams {
   int box_rows;  // keys per K/V box: gcd(block_size, 64), so a box never crosses a block
   int causal;    // 0: cross-attention (every row sees all of the tile's keys)
   int varlen;    // 1: K/V are contiguous [T, Hkv, D] tensors (3-D maps), no block table
+  // > 0 in a batch with query chunks: the SMs (n) split between this kernel
+  // and the decode kernel that follows and runs beside it.  CTAs with index
+  // >= n - decode_ctas leave at once, giving their SMs to it (the grid may
+  // be smaller than n when there are few tiles; then none leaves).
+  int split_ctas;
   float scale_log2;
 };
 

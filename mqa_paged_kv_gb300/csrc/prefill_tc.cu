@@ -159,6 +159,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // the tile list is written by the preceding kernel
+  if (p.split_ctas > 0) {
+    // The decode kernel of this batch may start now; CTAs past the prefill
+    // share leave their SMs to it.
+    griddep_launch_dependents();
+    if (blockIdx.x + p.hdr->decode_ctas >= static_cast<uint32_t>(p.split_ctas)) {
+      tc_fence_before();
+      __syncthreads();
+      if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+      return;
+    }
+  }
 
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
   const int TQ = p.tokens_per_tile / 2;  // tokens of one of the two Q tiles

@@ -146,10 +146,14 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   __shared__ int warp_sums[kWarps];
   __shared__ int dec_cnt[kDecBuckets];
   __shared__ int pf_cnt[kPfBuckets];
+  __shared__ double work[2];  // decode keys (per KV head), prefill (token, key) pairs (per head)
   const int tid = threadIdx.x;
   for (int i = tid; i < kDecBuckets; i += kThreads) dec_cnt[i] = 0;
   for (int i = tid; i < kPfBuckets; i += kThreads) pf_cnt[i] = 0;
-  if (tid == 0) p.hdr->status = 0;
+  if (tid == 0) {
+    p.hdr->status = 0;
+    work[0] = work[1] = 0.0;
+  }
   __syncthreads();
 
   // Pass 1: per-sequence plans, split offsets, bucket histograms.
@@ -160,6 +164,23 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     const int b = base + tid;
     const SeqPlan s = plan_seq(p, b);
     if (base == 0) first_plan = s;
+    if (p.split_ctas > 0) {  // the two kernels' work, for the SM split of a mixed batch
+      double dk = s.nsplit > 0 ? static_cast<double>(s.ctx) : 0.0;
+      double pk = 0.0;
+      if (s.ntile > 0) {
+        const double q = s.qlen, c = s.ctx;
+        pk = p.causal ? q * (c - q) + q * (q + 1.0) * 0.5 : q * c;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        dk += __shfl_xor_sync(0xffffffffu, dk, off);
+        pk += __shfl_xor_sync(0xffffffffu, pk, off);
+      }
+      if ((tid & 31) == 0) {
+        atomicAdd(&work[0], dk);
+        atomicAdd(&work[1], pk);
+      }
+    }
     int excl;
     const int tot = block_scan(s.nsplit, warp_sums, excl);
     if (s.bad) Status::raise(&p.hdr->status, PA_DEV_BAD_LENGTHS);
@@ -259,6 +280,25 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     h->prefill_grab = 0;
     h->prefill_tiles = static_cast<uint32_t>(tile_total);
     h->prefill_items = static_cast<uint32_t>(tile_total) * static_cast<uint32_t>(p.num_kv_heads);
+    // Batch with query chunks: the prefill kernel leaves k of the grid's SMs
+    // to the decode kernel, k / n about the decode kernel's share of the
+    // two kernels' estimated times.
+    uint32_t k = 0;
+    if (p.split_ctas > 0) {
+      const int n = p.split_ctas;
+      const double td = work[0] * p.num_kv_heads * p.head_dim * 4.0 / kDecodeBytesPerSmSec;
+      const double tp = work[1] * p.num_heads * p.head_dim * 4.0 / kPrefillFlopsPerSmSec;
+      if (td <= 0.0) {
+        k = 0;
+      } else if (tp <= 0.0) {
+        k = static_cast<uint32_t>(n);
+      } else {
+        int kk = static_cast<int>(n * td / (td + tp) * kDecodeShareMargin);
+        kk = kk < 1 ? 1 : (kk > n - 1 ? n - 1 : kk);
+        k = static_cast<uint32_t>(kk);
+      }
+    }
+    h->decode_ctas = k;
   }
   griddep_wait();
 }
