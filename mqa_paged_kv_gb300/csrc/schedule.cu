@@ -133,6 +133,10 @@ __device__ __forceinline__ int block_scan(int v, int* warp_sums, int& excl) {
 }
 }  // namespace
 
+// kSplit: the batch has query chunks and the grid is split between the
+// prefill and decode kernels (p.split_ctas > 0); a separate instance, so the
+// other calls run the work-list build without the estimate.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   griddep_launch_dependents();  // the attention kernel may start its prologue
   // The lengths this kernel reads are final before the previous kernel
@@ -146,13 +150,14 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   __shared__ int warp_sums[kWarps];
   __shared__ int dec_cnt[kDecBuckets];
   __shared__ int pf_cnt[kPfBuckets];
-  __shared__ double work[2];  // decode keys (per KV head), prefill (token, key) pairs (per head)
+  // Decode keys (per KV head) and prefill (token, key) pairs (per head).
+  __shared__ float work[kSplit ? 2 : 1];
   const int tid = threadIdx.x;
   for (int i = tid; i < kDecBuckets; i += kThreads) dec_cnt[i] = 0;
   for (int i = tid; i < kPfBuckets; i += kThreads) pf_cnt[i] = 0;
   if (tid == 0) {
     p.hdr->status = 0;
-    work[0] = work[1] = 0.0;
+    if constexpr (kSplit) work[0] = work[1] = 0.f;
   }
   __syncthreads();
 
@@ -164,12 +169,12 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     const int b = base + tid;
     const SeqPlan s = plan_seq(p, b);
     if (base == 0) first_plan = s;
-    if (p.split_ctas > 0) {  // the two kernels' work, for the SM split of a mixed batch
-      double dk = s.nsplit > 0 ? static_cast<double>(s.ctx) : 0.0;
-      double pk = 0.0;
+    if constexpr (kSplit) {  // the two kernels' work, for the SM split of a mixed batch
+      float dk = s.nsplit > 0 ? static_cast<float>(s.ctx) : 0.f;
+      float pk = 0.f;
       if (s.ntile > 0) {
-        const double q = s.qlen, c = s.ctx;
-        pk = p.causal ? q * (c - q) + q * (q + 1.0) * 0.5 : q * c;
+        const float q = static_cast<float>(s.qlen), c = static_cast<float>(s.ctx);
+        pk = p.causal ? q * (c - q) + q * (q + 1.f) * 0.5f : q * c;
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -283,22 +288,25 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     // Batch with query chunks: the prefill kernel leaves k of the grid's SMs
     // to the decode kernel, k / n about the decode kernel's share of the
     // two kernels' estimated times.
-    uint32_t k = 0;
-    if (p.split_ctas > 0) {
+    if constexpr (kSplit) {
+      uint32_t k = 0;
       const int n = p.split_ctas;
-      const double td = work[0] * p.num_kv_heads * p.head_dim * 4.0 / kDecodeBytesPerSmSec;
-      const double tp = work[1] * p.num_heads * p.head_dim * 4.0 / kPrefillFlopsPerSmSec;
-      if (td <= 0.0) {
+      const float td = work[0] * static_cast<float>(p.num_kv_heads * p.head_dim) *
+                       (4.f / static_cast<float>(kDecodeBytesPerSmSec));
+      const float tp = work[1] * static_cast<float>(p.num_heads * p.head_dim) *
+                       (4.f / static_cast<float>(kPrefillFlopsPerSmSec));
+      if (td <= 0.f) {
         k = 0;
-      } else if (tp <= 0.0) {
+      } else if (tp <= 0.f) {
         k = static_cast<uint32_t>(n);
       } else {
-        int kk = static_cast<int>(n * td / (td + tp) * kDecodeShareMargin);
+        int kk = static_cast<int>(static_cast<float>(n) * td / (td + tp) *
+                                  static_cast<float>(kDecodeShareMargin));
         kk = kk < 1 ? 1 : (kk > n - 1 ? n - 1 : kk);
         k = static_cast<uint32_t>(kk);
       }
+      h->decode_ctas = k;
     }
-    h->decode_ctas = k;
   }
   griddep_wait();
 }
@@ -314,7 +322,8 @@ int launch_prepare(const PrepareParams& p, bool /*bf16*/, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prepare_kernel, p) == cudaSuccess ? 1 : -1;
+  return cudaLaunchKernelEx(&cfg, p.split_ctas > 0 ? prepare_kernel<true> : prepare_kernel<false>,
+                            p) == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace pa
