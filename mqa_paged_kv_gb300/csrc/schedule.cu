@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
                        (4.f / static_cast<float>(kDecodeBytesPerSmSec));
       const float tp = work[1] * static_cast<float>(p.num_heads * p.head_dim) *
                        (4.f / static_cast<float>(kPrefillFlopsPerSmSec));
-      if (td <= 0.f) {
+      if (td <= 0.f || n < 2) {  // nothing to split (one CTA: the prefill CTA stays)
         k = 0;
       } else if (tp <= 0.f) {
         k = static_cast<uint32_t>(n);

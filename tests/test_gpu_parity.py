@@ -406,14 +406,16 @@ def test_varlen_prefill_workload_sampled_rows():
     _run_varlen(c, rows=rows)
 
 
-def test_cta_limit_gives_the_same_bits():
-    # fewer persistent CTAs only change which SM runs which item
+@pytest.mark.parametrize("limit", [1, 7])
+def test_cta_limit_gives_the_same_bits(limit):
+    # fewer persistent CTAs only change which SM runs which item (one CTA:
+    # the mixed call does not split the SMs between its two kernels)
     c = W.mixed_prefill_decode(5, n_prefill=4, n_decode=12, q_range=(40, 200),
                                prior_range=(0, 600), dec_range=(64, 1500))
     g = GpuCase(c)
     g.write_cache()
     ref = bits(g.attention())
-    g.pa.pa_limit_next_call_ctas(7)
+    g.pa.pa_limit_next_call_ctas(limit)
     out = g.attention()
     torch.cuda.synchronize()
     assert np.array_equal(bits(out), ref)
