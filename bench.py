@@ -521,8 +521,10 @@ def measure_varlen(seed: int, device, steps: int, warmup: int, flush):
 
 def measure_two_kernel(seed: int, device, steps: int, warmup: int, flush, block_size: int = 16):
     """The mixed batch two ways, attention only, cache already written:
-    (a) the fused call (one work list, prefill and decode kernels back to
-    back on one stream); (b) the arrangement of vLLM PR #14431's op: a
+    (a) the library's one call (one work list; the prefill kernel and the
+    decode kernel resident side by side, the decode kernel on the SM share
+    the work list gives it and on each SM the prefill kernel frees); (b) the
+    arrangement of vLLM PR #14431's op: a
     prefill call over the query chunks only and a decode call over the
     decode rows on a second stream, concurrently, with the SMs split between
     them (pa_limit_next_call_ctas); every split in `splits` is timed."""
