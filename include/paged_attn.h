@@ -156,6 +156,14 @@ PA_API size_t paged_attn_chunked_prefill_workspace_bytes(
  *   host-known bounds the launch is sized by (no device sync); rows of
  *   sequences with qlen = 1 follow the decode path (with KV splits as in
  *   paged_attn_decode), the rest the prefill path.
+ *
+ *   Scheduling, all on `stream` and on the device (no host sync): a
+ *   work-list kernel sorts the rows into the two paths and, from their key
+ *   counts, sizes the decode path's share of the SMs; the prefill kernel
+ *   and the decode kernel then run side by side, the decode kernel taking
+ *   that share at once and each SM the prefill kernel frees later.  The
+ *   call's kernels finish, and its outputs are written, before work queued
+ *   after it on `stream` starts.
  */
 PA_API int paged_attn_chunked_prefill(const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,
@@ -289,8 +297,9 @@ PA_API void pa_profile_next_call(void* start_event, void* stop_event);
  * of the next attention call made on this host thread (decode, chunked
  * prefill, cross-attention or varlen prefill), so that two calls on two
  * streams can run side by side on disjoint SMs; max_ctas <= 0 clears it.
- * The cap is consumed by that call.  The pages define no such call: it
- * exists to compare one fused mixed-batch launch with a prefill call and a
+ * The cap is consumed by that call; a mixed call splits its capped SMs
+ * between its two paths as above.  The pages define no such call: it
+ * exists to compare one mixed-batch call with a prefill call and a
  * concurrent decode call, the two-kernel arrangement of vLLM PR #14431's
  * op (review thread on chunked_prefill_paged_decode.py).
  */
