@@ -157,6 +157,34 @@ def test_golden_powers_of_two():
     np.testing.assert_allclose(o64[0], np.array(g["expected"]), rtol=0, atol=1e-13)
 
 
+def test_golden_causal_chunk_bottom_right():
+    # hand-derived: a two-token chunk after a one-token prefix; the expected
+    # rows differ from those of a top-left mask (see the fixture's derivation)
+    with open(os.path.join(GOLDEN, "causal_chunk_bottom_right.json")) as f:
+        g = json.load(f)
+    Hq, Hkv, D, bs = g["num_heads"], g["num_kv_heads"], g["head_dim"], g["block_size"]
+    ctx, qlen = g["context_len"], g["query_len"]
+    bt = np.array([g["block_table"]], np.int32)
+    kc = np.full((2, Hkv, bs, D), 0x7FC0, np.uint16)  # NaN everywhere else
+    vc = kc.copy()
+    keys = np.array(g["keys"], np.float32)      # [Hkv, ctx, D]
+    vals = np.array(g["values"], np.float32)
+    for j in range(ctx):
+        blk = bt[0, j // bs]
+        kc[blk, :, j % bs] = W.f32_to_bits(keys[:, j], W.BF16)
+        vc[blk, :, j % bs] = W.f32_to_bits(vals[:, j], W.BF16)
+    q = W.f32_to_bits(np.array(g["queries"], np.float32), W.BF16)   # [qlen, Hq, D]
+    assert q.shape == (qlen, Hq, D)
+    o64, ob = oracle.paged_attention(q, kc, vc, bt, np.array([0, qlen], np.int32),
+                                     np.array([ctx], np.int32), math.log(2.0), Hkv, W.BF16)
+    np.testing.assert_allclose(o64, np.array(g["expected"]), rtol=0, atol=1e-13)
+    # every expected value but 4.2 and 16.8 is a bf16 value: those round exactly
+    exact = np.array(g["expected"])
+    ok = W.f32_to_bits(exact.astype(np.float32), W.BF16)
+    same = (exact == W.bits_to_f32(ok, W.BF16))
+    assert np.array_equal(ob[same], ok[same])
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("hq,hkv", [(4, 2), (6, 1), (3, 3), (8, 2)])
 def test_brute_force_decode(seed, hq, hkv):
