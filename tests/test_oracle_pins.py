@@ -2,7 +2,7 @@
 
 Each test ties the oracle to something other than itself: IEEE rounding as
 implemented by numpy/torch, a dense brute-force loop written here, PyTorch's
-float64 scaled_dot_product_attention, closed forms, a hand-derived fixture and
+float64 scaled_dot_product_attention, closed forms, hand-derived fixtures and
 invariants of paged GQA attention.  A dropped term, a wrong head map, a wrong
 causal offset or a transposed operand in the oracle fails at least one.
 """
@@ -135,44 +135,52 @@ def _brute_force(case):
 # attention pins
 # --------------------------------------------------------------------------
 
-def test_golden_powers_of_two():
-    with open(os.path.join(GOLDEN, "gqa_powers_of_two.json")) as f:
+def _golden(name):
+    """A hand-derived fixture and its paged cache (one sequence, NaN in every
+    slot past the context)."""
+    with open(os.path.join(GOLDEN, name)) as f:
         g = json.load(f)
-    Hq, Hkv, D, bs = g["num_heads"], g["num_kv_heads"], g["head_dim"], g["block_size"]
-    ctx = g["context_len"]
+    Hkv, D, bs = g["num_kv_heads"], g["head_dim"], g["block_size"]
     bt = np.array([g["block_table"]], np.int32)
-    NB = 2
-    kc = np.full((NB, Hkv, bs, D), 0x7FC0, np.uint16)  # NaN everywhere else
+    kc = np.full((bt.shape[1], Hkv, bs, D), 0x7FC0, np.uint16)
     vc = kc.copy()
     keys = np.array(g["keys"], np.float32)      # [Hkv, ctx, D]
     vals = np.array(g["values"], np.float32)
-    for j in range(ctx):
+    for j in range(g["context_len"]):
         blk = bt[0, j // bs]
         kc[blk, :, j % bs] = W.f32_to_bits(keys[:, j], W.BF16)
         vc[blk, :, j % bs] = W.f32_to_bits(vals[:, j], W.BF16)
+    return g, kc, vc, bt
+
+
+def test_golden_powers_of_two():
+    g, kc, vc, bt = _golden("gqa_powers_of_two.json")
     q = W.f32_to_bits(np.array(g["queries"], np.float32)[None], W.BF16)
     o64, ob = oracle.paged_attention(q, kc, vc, bt, np.array([0, 1], np.int32),
-                                     np.array([ctx], np.int32), math.log(2.0),
-                                     Hkv, W.BF16)
+                                     np.array([g["context_len"]], np.int32), math.log(2.0),
+                                     g["num_kv_heads"], W.BF16)
     np.testing.assert_allclose(o64[0], np.array(g["expected"]), rtol=0, atol=1e-13)
+
+
+def test_golden_cross_attention_unmasked():
+    # hand-derived: four decoder rows over three encoder keys, no mask
+    g, kc, vc, bt = _golden("cross_attention_unmasked.json")
+    q = W.f32_to_bits(np.array(g["queries"], np.float32), W.BF16)
+    assert q.shape == (g["query_len"], g["num_heads"], g["head_dim"])
+    o64, ob = oracle.cross_attention(q, kc, vc, bt, np.array([0, g["query_len"]], np.int32),
+                                     np.array([g["context_len"]], np.int32), math.log(2.0),
+                                     g["num_kv_heads"], W.BF16)
+    exact = np.array(g["expected"])
+    np.testing.assert_allclose(o64, exact, rtol=0, atol=1e-13)
+    assert np.array_equal(ob, W.f32_to_bits(exact.astype(np.float32), W.BF16))
 
 
 def test_golden_causal_chunk_bottom_right():
     # hand-derived: a two-token chunk after a one-token prefix; the expected
     # rows differ from those of a top-left mask (see the fixture's derivation)
-    with open(os.path.join(GOLDEN, "causal_chunk_bottom_right.json")) as f:
-        g = json.load(f)
-    Hq, Hkv, D, bs = g["num_heads"], g["num_kv_heads"], g["head_dim"], g["block_size"]
+    g, kc, vc, bt = _golden("causal_chunk_bottom_right.json")
+    Hq, Hkv, D = g["num_heads"], g["num_kv_heads"], g["head_dim"]
     ctx, qlen = g["context_len"], g["query_len"]
-    bt = np.array([g["block_table"]], np.int32)
-    kc = np.full((2, Hkv, bs, D), 0x7FC0, np.uint16)  # NaN everywhere else
-    vc = kc.copy()
-    keys = np.array(g["keys"], np.float32)      # [Hkv, ctx, D]
-    vals = np.array(g["values"], np.float32)
-    for j in range(ctx):
-        blk = bt[0, j // bs]
-        kc[blk, :, j % bs] = W.f32_to_bits(keys[:, j], W.BF16)
-        vc[blk, :, j % bs] = W.f32_to_bits(vals[:, j], W.BF16)
     q = W.f32_to_bits(np.array(g["queries"], np.float32), W.BF16)   # [qlen, Hq, D]
     assert q.shape == (qlen, Hq, D)
     o64, ob = oracle.paged_attention(q, kc, vc, bt, np.array([0, qlen], np.int32),
