@@ -193,6 +193,20 @@ def test_golden_causal_chunk_bottom_right():
     assert np.array_equal(ob[same], ok[same])
 
 
+def test_golden_causal_chunk_varlen_contiguous_kv():
+    # the same hand-derived rows through the varlen definition: the three
+    # keys as contiguous K/V of one sequence, its two query rows the chunk
+    with open(os.path.join(GOLDEN, "causal_chunk_bottom_right.json")) as f:
+        g = json.load(f)
+    k = W.f32_to_bits(np.array(g["keys"], np.float32).transpose(1, 0, 2), W.BF16)  # [ctx, Hkv, D]
+    v = W.f32_to_bits(np.array(g["values"], np.float32).transpose(1, 0, 2), W.BF16)
+    q = W.f32_to_bits(np.array(g["queries"], np.float32), W.BF16)
+    o64, _ = oracle.varlen_attention(q, k, v, np.array([0, g["query_len"]], np.int32),
+                                     np.array([0, g["context_len"]], np.int32),
+                                     math.log(2.0), W.BF16)
+    np.testing.assert_allclose(o64, np.array(g["expected"]), rtol=0, atol=1e-13)
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("hq,hkv", [(4, 2), (6, 1), (3, 3), (8, 2)])
 def test_brute_force_decode(seed, hq, hkv):
