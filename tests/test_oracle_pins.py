@@ -381,6 +381,23 @@ def test_split_combine_identity(S):
         assert np.any(np.isneginf(pl))
 
 
+def test_lse_combine_hand_values():
+    # Split weights are e^(lse_s - max): lse 0 and ln 3 weigh 1 : 3, so
+    # partials (4, 0) and (0, 4) merge to (1, 3); an empty split (lse -inf)
+    # weighs nothing, whatever its partial holds; a common shift of every
+    # lse changes nothing (here 1000, past exp's range without the max);
+    # all splits empty gives zeros.
+    inf = float("inf")
+    po = np.array([[[4.0, 0.0], [0.0, 4.0], [1e9, -1e9]],
+                   [[4.0, 0.0], [0.0, 4.0], [7.0, 7.0]],
+                   [[5.0, 5.0], [6.0, 6.0], [7.0, 7.0]]])
+    pl = np.array([[0.0, math.log(3.0), -inf],
+                   [1000.0, 1000.0 + math.log(3.0), -inf],
+                   [-inf, -inf, -inf]])
+    out = oracle.lse_combine(po, pl)
+    np.testing.assert_allclose(out, [[1.0, 3.0], [1.0, 3.0], [0.0, 0.0]], rtol=0, atol=1e-12)
+
+
 def test_split_lse_closed_form():
     # one key per split: lse of split s is exactly its scaled logit
     c = _small_case(seed=12, B=1, Hq=2, Hkv=1, D=8, bs=4, ctx=np.array([8]))
