@@ -135,61 +135,67 @@ def _brute_force(case):
 # attention pins
 # --------------------------------------------------------------------------
 
-def _golden(name):
+def _golden(name, dtype=W.BF16):
     """A hand-derived fixture and its paged cache (one sequence, NaN in every
-    slot past the context)."""
+    slot past the context).  Every key, value and query in the fixtures is
+    exact in fp16 and bf16 alike."""
     with open(os.path.join(GOLDEN, name)) as f:
         g = json.load(f)
     Hkv, D, bs = g["num_kv_heads"], g["head_dim"], g["block_size"]
     bt = np.array([g["block_table"]], np.int32)
-    kc = np.full((bt.shape[1], Hkv, bs, D), 0x7FC0, np.uint16)
+    kc = np.full((bt.shape[1], Hkv, bs, D), W.NAN_BITS[dtype], np.uint16)
     vc = kc.copy()
     keys = np.array(g["keys"], np.float32)      # [Hkv, ctx, D]
     vals = np.array(g["values"], np.float32)
     for j in range(g["context_len"]):
         blk = bt[0, j // bs]
-        kc[blk, :, j % bs] = W.f32_to_bits(keys[:, j], W.BF16)
-        vc[blk, :, j % bs] = W.f32_to_bits(vals[:, j], W.BF16)
+        kc[blk, :, j % bs] = W.f32_to_bits(keys[:, j], dtype)
+        vc[blk, :, j % bs] = W.f32_to_bits(vals[:, j], dtype)
     return g, kc, vc, bt
 
 
-def test_golden_powers_of_two():
-    g, kc, vc, bt = _golden("gqa_powers_of_two.json")
-    q = W.f32_to_bits(np.array(g["queries"], np.float32)[None], W.BF16)
+@pytest.mark.parametrize("dtype", [W.BF16, W.F16])
+def test_golden_powers_of_two(dtype):
+    g, kc, vc, bt = _golden("gqa_powers_of_two.json", dtype)
+    q = W.f32_to_bits(np.array(g["queries"], np.float32)[None], dtype)
     o64, ob = oracle.paged_attention(q, kc, vc, bt, np.array([0, 1], np.int32),
                                      np.array([g["context_len"]], np.int32), math.log(2.0),
-                                     g["num_kv_heads"], W.BF16)
+                                     g["num_kv_heads"], dtype)
     np.testing.assert_allclose(o64[0], np.array(g["expected"]), rtol=0, atol=1e-13)
 
 
-def test_golden_cross_attention_unmasked():
+@pytest.mark.parametrize("dtype", [W.BF16, W.F16])
+def test_golden_cross_attention_unmasked(dtype):
     # hand-derived: four decoder rows over three encoder keys, no mask
-    g, kc, vc, bt = _golden("cross_attention_unmasked.json")
-    q = W.f32_to_bits(np.array(g["queries"], np.float32), W.BF16)
+    g, kc, vc, bt = _golden("cross_attention_unmasked.json", dtype)
+    q = W.f32_to_bits(np.array(g["queries"], np.float32), dtype)
     assert q.shape == (g["query_len"], g["num_heads"], g["head_dim"])
     o64, ob = oracle.cross_attention(q, kc, vc, bt, np.array([0, g["query_len"]], np.int32),
                                      np.array([g["context_len"]], np.int32), math.log(2.0),
-                                     g["num_kv_heads"], W.BF16)
+                                     g["num_kv_heads"], dtype)
     exact = np.array(g["expected"])
     np.testing.assert_allclose(o64, exact, rtol=0, atol=1e-13)
-    assert np.array_equal(ob, W.f32_to_bits(exact.astype(np.float32), W.BF16))
+    assert np.array_equal(ob, W.f32_to_bits(exact.astype(np.float32), dtype))
 
 
-def test_golden_causal_chunk_bottom_right():
+@pytest.mark.parametrize("dtype", [W.BF16, W.F16])
+def test_golden_causal_chunk_bottom_right(dtype):
     # hand-derived: a two-token chunk after a one-token prefix; the expected
     # rows differ from those of a top-left mask (see the fixture's derivation)
-    g, kc, vc, bt = _golden("causal_chunk_bottom_right.json")
+    g, kc, vc, bt = _golden("causal_chunk_bottom_right.json", dtype)
     Hq, Hkv, D = g["num_heads"], g["num_kv_heads"], g["head_dim"]
     ctx, qlen = g["context_len"], g["query_len"]
-    q = W.f32_to_bits(np.array(g["queries"], np.float32), W.BF16)   # [qlen, Hq, D]
+    q = W.f32_to_bits(np.array(g["queries"], np.float32), dtype)   # [qlen, Hq, D]
     assert q.shape == (qlen, Hq, D)
     o64, ob = oracle.paged_attention(q, kc, vc, bt, np.array([0, qlen], np.int32),
-                                     np.array([ctx], np.int32), math.log(2.0), Hkv, W.BF16)
+                                     np.array([ctx], np.int32), math.log(2.0), Hkv, dtype)
     np.testing.assert_allclose(o64, np.array(g["expected"]), rtol=0, atol=1e-13)
-    # every expected value but 4.2 and 16.8 is a bf16 value: those round exactly
+    # every expected value but 4.2 and 16.8 is exact in the element type:
+    # those round to themselves
     exact = np.array(g["expected"])
-    ok = W.f32_to_bits(exact.astype(np.float32), W.BF16)
-    same = (exact == W.bits_to_f32(ok, W.BF16))
+    ok = W.f32_to_bits(exact.astype(np.float32), dtype)
+    same = (exact == W.bits_to_f32(ok, dtype))
+    assert same.sum() == exact.size - 2
     assert np.array_equal(ob[same], ok[same])
 
 
