@@ -132,18 +132,72 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+# The C ABI sees raw pointers and sizes only, so the binding checks what a
+# pointer cannot carry -- device, integer width, matching shapes -- before any
+# allocation or launch: a host tensor, an int64 table or a short lengths
+# array would otherwise reach the kernels as a bad address or a misread.
+def _expect(ok: bool, msg: str) -> None:
+    if not ok:
+        raise ValueError(msg)
+
+
+def _same_device(ref: torch.Tensor, **named) -> None:
+    _expect(ref.device.type == "cuda", f"tensors must be CUDA tensors (got {ref.device})")
+    for name, t in named.items():
+        if t is not None:
+            _expect(t.device == ref.device, f"{name} is on {t.device}, expected {ref.device}")
+
+
+def _int32(**named) -> None:
+    for name, t in named.items():
+        _expect(t.dtype == torch.int32, f"{name} must be int32 (got {t.dtype})")
+
+
+def _check_paged(q, k_cache, v_cache, block_tables, context_lens, out, workspace,
+                 cu_query_lens=None) -> None:
+    """Shapes and types shared by the paged attention calls: q [T, Hq, D],
+    caches [NB, Hkv, bs, D] of q's type, block_tables [B, MBS] and
+    context_lens [B] int32, cu_query_lens [B + 1] int32, out like q."""
+    _expect(q.dim() == 3 and k_cache.dim() == 4, "q must be [T, Hq, D], caches [NB, Hkv, bs, D]")
+    _expect(v_cache.shape == k_cache.shape and k_cache.shape[3] == q.shape[2],
+            "k_cache and v_cache must have one shape whose last dim is q's head_dim")
+    _expect(k_cache.dtype == q.dtype and v_cache.dtype == q.dtype, "caches must have q's dtype")
+    _int32(block_tables=block_tables, context_lens=context_lens)
+    B = context_lens.shape[0]
+    _expect(context_lens.dim() == 1 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+            "block_tables must be [B, max_blocks] and context_lens [B]")
+    if cu_query_lens is None:
+        _expect(q.shape[0] == B, "decode takes one query row per sequence")
+    else:
+        _int32(cu_query_lens=cu_query_lens)
+        _expect(cu_query_lens.shape == (B + 1,), "cu_query_lens must be [B + 1]")
+    if out is not None:
+        _expect(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _same_device(q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+                 context_lens=context_lens, cu_query_lens=cu_query_lens, out=out,
+                 workspace=workspace)
+
+
 def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
                       v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                       status_word: Optional[torch.Tensor] = None, stream=None) -> None:
     """k, v [T, Hkv, D] -> k_cache, v_cache [NB, Hkv, bs, D] at slot_mapping
     (int64, -1 skips)."""
     _contig(k, v, k_cache, v_cache, slot_mapping)
+    _expect(status_word is None
+            or status_word.dtype in (torch.int32, getattr(torch, "uint32", None)),
+            "status_word must be a 32-bit integer tensor")
+    _expect(k.dim() == 3 and k_cache.dim() == 4 and slot_mapping.shape == (k.shape[0],),
+            "k, v must be [T, Hkv, D], caches [NB, Hkv, bs, D], slot_mapping [T]")
     T, Hkv, D = k.shape
     NB, Hkv2, bs, D2 = k_cache.shape
     if Hkv2 != Hkv or D2 != D or v.shape != k.shape or v_cache.shape != k_cache.shape:
         raise ValueError("shape mismatch")
-    if slot_mapping.dtype != torch.int64 or k.dtype != k_cache.dtype:
+    if slot_mapping.dtype != torch.int64 or not (k.dtype == v.dtype == k_cache.dtype
+                                                 == v_cache.dtype):
         raise ValueError("slot_mapping must be int64 and caches match k's dtype")
+    _same_device(k, v=v, k_cache=k_cache, v_cache=v_cache, slot_mapping=slot_mapping,
+                 status_word=status_word)
     rc = _lib.reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                 _ptr(slot_mapping), T, Hkv, D, bs, NB, _dtype_code(k),
                                 _ptr(status_word), _stream(stream))
@@ -178,6 +232,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     """q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables [B, MBS] int32;
     context_lens [B] int32 -> out [B, Hq, D]."""
     _contig(q, k_cache, v_cache, block_tables, context_lens, out)
+    _check_paged(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
     B, Hq, D = q.shape
     NB, Hkv, bs, _ = k_cache.shape
     mbs = block_tables.shape[1]
@@ -202,6 +257,8 @@ def paged_attn_chunked_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
                                stream=None) -> torch.Tensor:
     """q [T, Hq, D] in the cu_query_lens layout -> out [T, Hq, D]."""
     _contig(q, k_cache, v_cache, block_tables, cu_query_lens, context_lens, out)
+    _check_paged(q, k_cache, v_cache, block_tables, context_lens, out, workspace,
+                 cu_query_lens=cu_query_lens)
     T, Hq, D = q.shape
     NB, Hkv, bs, _ = k_cache.shape
     B = context_lens.shape[0]
@@ -229,6 +286,8 @@ def paged_attn_cross_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
     """Decoder rows q [T, Hq, D] (cu_query_lens layout) over a static encoder
     cache; context_lens = encoder tokens per sequence; no causal mask."""
     _contig(q, k_cache, v_cache, block_tables, cu_query_lens, context_lens, out)
+    _check_paged(q, k_cache, v_cache, block_tables, context_lens, out, workspace,
+                 cu_query_lens=cu_query_lens)
     T, Hq, D = q.shape
     NB, Hkv, bs, _ = k_cache.shape
     B = context_lens.shape[0]
@@ -260,6 +319,15 @@ def gqa_varlen_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     """q [Tq, Hq, D], k, v [Tk, Hkv, D] contiguous; cu_seqlens int32 [B+1]
     -> out [Tq, Hq, D] (bottom-right causal per sequence, no cache)."""
     _contig(q, k, v, cu_seqlens_q, cu_seqlens_k, out)
+    _expect(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape and k.shape[2] == q.shape[2],
+            "q must be [Tq, Hq, D], k and v [Tk, Hkv, D]")
+    _expect(k.dtype == q.dtype and v.dtype == q.dtype, "k and v must have q's dtype")
+    _int32(cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k)
+    _expect(cu_seqlens_q.dim() == 1 and cu_seqlens_k.shape == cu_seqlens_q.shape,
+            "cu_seqlens_q and cu_seqlens_k must both be [B + 1]")
+    _expect(out is None or (out.shape == q.shape and out.dtype == q.dtype), "out must match q")
+    _same_device(q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k, out=out,
+                 workspace=workspace)
     Tq, Hq, D = q.shape
     Tk, Hkv, _ = k.shape
     B = cu_seqlens_q.shape[0] - 1
@@ -277,6 +345,7 @@ def gqa_varlen_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 
 def pa_read_device_status(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:
+    _same_device(workspace)
     flags = ctypes.c_uint32(0)
     rc = _lib.pa_read_device_status(_ptr(workspace), int(bool(clear)), ctypes.byref(flags),
                                     _stream(stream))

@@ -144,3 +144,91 @@ def test_cta_limit_is_a_host_setting(lib):
     # no device call: the cap is only stored for the next attention call
     lib.pa_limit_next_call_ctas(32)
     lib.pa_limit_next_call_ctas(0)
+
+
+# The binding rejects, on the host and before any allocation or launch, what
+# a raw pointer cannot carry: shapes that disagree, integer widths, element
+# types and host (non-CUDA) tensors.  CPU tensors suffice to reach each check.
+def _paged_args(B=4, Hq=8, Hkv=2, D=64, NB=16, bs=16, mbs=4, dt=None):
+    import torch
+    dt = dt or torch.bfloat16
+    return dict(q=torch.zeros(B, Hq, D, dtype=dt), k_cache=torch.zeros(NB, Hkv, bs, D, dtype=dt),
+                v_cache=torch.zeros(NB, Hkv, bs, D, dtype=dt),
+                block_tables=torch.zeros(B, mbs, dtype=torch.int32),
+                context_lens=torch.ones(B, dtype=torch.int32))
+
+
+def _decode_call(lib, a):
+    return lib.paged_attn_decode(a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
+                                 a["context_lens"], 0.125, out=a.get("out"))
+
+
+@pytest.mark.parametrize("change,msg", [
+    (lambda a, t: a.update(block_tables=a["block_tables"].long()), "int32"),
+    (lambda a, t: a.update(context_lens=a["context_lens"].long()), "int32"),
+    (lambda a, t: a.update(context_lens=a["context_lens"][:3].clone()), "block_tables"),
+    (lambda a, t: a.update(block_tables=a["block_tables"][:3].clone()), "block_tables"),
+    (lambda a, t: a.update(q=a["q"][:3].clone()), "one query row"),
+    (lambda a, t: a.update(v_cache=a["v_cache"][:8].clone()), "one shape"),
+    (lambda a, t: a.update(k_cache=a["k_cache"].half(), v_cache=a["v_cache"].half()), "dtype"),
+    (lambda a, t: a.update(out=t.zeros(4, 8, 64, dtype=t.float16)), "out must match"),
+    (lambda a, t: a.update(out=t.zeros(4, 8, 32, dtype=t.bfloat16)), "out must match"),
+    (lambda a, t: None, "CUDA tensors"),     # valid shapes, but on the host
+])
+def test_binding_rejects_mismatched_decode_tensors(lib, change, msg):
+    import torch
+    a = _paged_args()
+    change(a, torch)
+    with pytest.raises(ValueError, match=msg):
+        _decode_call(lib, a)
+    assert lib.last_launch_count() == 0
+
+
+def test_binding_rejects_mismatched_chunked_tensors(lib):
+    import torch
+    a = _paged_args()
+    for cu, msg in ((torch.tensor([0, 1, 2, 3, 4]).long(), "int32"),
+                    (torch.tensor([0, 1, 2, 4], dtype=torch.int32), r"\[B \+ 1\]"),
+                    (torch.tensor([0, 1, 2, 3, 4], dtype=torch.int32), "CUDA tensors")):
+        for f in (lib.paged_attn_chunked_prefill, lib.paged_attn_cross_attention):
+            with pytest.raises(ValueError, match=msg):
+                f(a["q"], a["k_cache"], a["v_cache"], a["block_tables"], cu,
+                  a["context_lens"], 1, 0.125)
+
+
+def test_binding_rejects_mismatched_cache_write(lib):
+    import torch
+    k = torch.zeros(5, 2, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(16, 2, 16, 64, dtype=torch.bfloat16)
+    sm = torch.zeros(5, dtype=torch.int64)
+    with pytest.raises(ValueError, match="slot_mapping"):
+        lib.reshape_and_cache(k, k.clone(), kc, kc.clone(), sm[:4].clone())
+    with pytest.raises(ValueError, match="int64"):
+        lib.reshape_and_cache(k, k.clone(), kc, kc.clone(), sm.int())
+    with pytest.raises(ValueError, match="dtype"):
+        lib.reshape_and_cache(k, k.half(), kc, kc.clone(), sm)
+    with pytest.raises(ValueError, match="32-bit"):
+        lib.reshape_and_cache(k, k.clone(), kc, kc.clone(), sm,
+                              status_word=torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        lib.reshape_and_cache(k, k.clone(), kc, kc.clone(), sm)
+
+
+def test_binding_rejects_mismatched_varlen_tensors(lib):
+    import torch
+    q = torch.zeros(10, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(12, 2, 64, dtype=torch.bfloat16)
+    cq = torch.tensor([0, 4, 10], dtype=torch.int32)
+    ck = torch.tensor([0, 5, 12], dtype=torch.int32)
+    with pytest.raises(ValueError, match="int32"):
+        lib.gqa_varlen_prefill(q, k, k.clone(), cq.long(), ck, 6, 0.125)
+    with pytest.raises(ValueError, match=r"\[B \+ 1\]"):
+        lib.gqa_varlen_prefill(q, k, k.clone(), cq, ck[:2].clone(), 6, 0.125)
+    with pytest.raises(ValueError, match="k and v"):
+        lib.gqa_varlen_prefill(q, k, k[:11].clone(), cq, ck, 6, 0.125)
+    with pytest.raises(ValueError, match="dtype"):
+        lib.gqa_varlen_prefill(q, k.half(), k.half(), cq, ck, 6, 0.125)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        lib.gqa_varlen_prefill(q, k, k.clone(), cq, ck, 6, 0.125)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        lib.pa_read_device_status(torch.zeros(256, dtype=torch.uint8))
