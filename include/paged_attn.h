@@ -84,8 +84,13 @@ typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEV_BAD_BLOCK_ID 0x1u  /* a block-table entry outside [0, NB) */
 #define PA_DEV_BAD_SLOT 0x2u      /* a slot_mapping entry outside [-1, NB*bs) */
 #define PA_DEV_WAIT_TIMEOUT 0x4u  /* a pipeline wait ran out of time */
-#define PA_DEV_BAD_LENGTHS 0x8u   /* a sequence with ctx < 0, ctx > mbs * bs,
-                                     qlen < 0 or qlen > ctx: skipped */
+#define PA_DEV_BAD_LENGTHS 0x8u   /* a sequence with ctx < 0, ctx > mbs * bs
+                                     or qlen > ctx: skipped.  A query range
+                                     outside [0, total_query_tokens) or with
+                                     qlen < 0 (cu_query_lens not
+                                     non-decreasing within the token count):
+                                     the whole call does no work, since the
+                                     other ranges may overlap */
 
 /* Human-readable name of a pa_status value (static string). */
 PA_API const char* pa_status_string(int status);

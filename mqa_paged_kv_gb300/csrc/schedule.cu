@@ -25,10 +25,11 @@ struct SeqPlan {
   int nsplit, chunk_keys;  // decode
   int ntile;               // prefill
   bool bad;                // lengths outside the contract: no work, flagged
+  bool bad_rows;           // query rows outside [0, total) or a negative count
 };
 
 __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
-  SeqPlan s{0, 0, 0, 0, 0, 0, 0, false};
+  SeqPlan s{0, 0, 0, 0, 0, 0, 0, false, false};
   if (b >= p.num_seqs) return s;
   if (p.cu_key_lens) {  // contiguous K/V of a varlen batch
     s.kbase = p.cu_key_lens[b];
@@ -48,6 +49,7 @@ __device__ __forceinline__ SeqPlan plan_seq(const PrepareParams& p, int b) {
   if (ctx < 0 || ctx > max_ctx || s.kbase < 0 || s.qlen < 0 || (p.causal && s.qlen > ctx && ctx > 0) || s.tok < 0 ||
       static_cast<int64_t>(s.tok) + s.qlen > p.total_tokens) {
     s.bad = true;
+    s.bad_rows = s.qlen < 0 || s.tok < 0 || static_cast<int64_t>(s.tok) + s.qlen > p.total_tokens;
     s.qlen = 0;
     return s;
   }
@@ -164,11 +166,13 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   // Pass 1: per-sequence plans, split offsets, bucket histograms.
   int carry = 0, tile_total = 0;
   int first_split_offset = 0;  // this thread's sequence in the first pass
-  SeqPlan first_plan{0, 0, 0, 0, 0, 0, 0, false};  // ... and its plan (pass 2 reuses it)
+  SeqPlan first_plan{0, 0, 0, 0, 0, 0, 0, false, false};  // ... and its plan (pass 2 reuses it)
+  bool any_bad_rows = false;
   for (int base = 0; base < p.num_seqs; base += kThreads) {
     const int b = base + tid;
     const SeqPlan s = plan_seq(p, b);
     if (base == 0) first_plan = s;
+    any_bad_rows |= s.bad_rows;
     if constexpr (kSplit) {  // the two kernels' work, for the SM split of a mixed batch
       float dk = s.nsplit > 0 ? static_cast<float>(s.ctx) : 0.f;
       float pk = 0.f;
@@ -214,7 +218,13 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
     tile_total += block_scan(s.ntile, warp_sums, tex);
     carry += tot;
   }
-  __syncthreads();
+  // Query rows are disjoint and inside [0, total) only if every sequence's
+  // range is (cu_query_lens non-decreasing, within the token count).  One
+  // range outside that means the offsets themselves are wrong, and the other
+  // sequences' ranges may overlap: their tiles and splits could then outgrow
+  // the workspace, which is sized for disjoint rows.  Such a call does no
+  // work at all (the sequences at fault are flagged).
+  const bool bad_rows = __syncthreads_or(any_bad_rows) != 0;
 
   // Bucket starts, longest first: scan the reversed histograms.
   {
@@ -234,7 +244,19 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   __syncthreads();
 
   // Pass 2: emit the sorted lists and zero the rows of key-less sequences.
-  for (int base = 0; base < p.num_seqs; base += kThreads) {
+  if (bad_rows) {  // no lists; no sequence left for the split combine
+    for (int b = tid; b < p.num_seqs; b += kThreads) {
+      SeqInfo si;
+      si.split_offset = 0;
+      si.nsplit = 0;
+      si.tok = 0;
+      si.qlen = 0;
+      p.seq_info[b] = si;
+    }
+    carry = 0;
+    tile_total = 0;
+  }
+  for (int base = 0; !bad_rows && base < p.num_seqs; base += kThreads) {
     const int b = base + tid;
     // All lanes take part in the warp aggregation.  When one pass covers the
     // batch the plan of pass 1 is still in registers: no second read of the
