@@ -232,3 +232,24 @@ def test_binding_rejects_mismatched_varlen_tensors(lib):
         lib.gqa_varlen_prefill(q, k, k.clone(), cq, ck, 6, 0.125)
     with pytest.raises(ValueError, match="CUDA tensors"):
         lib.pa_read_device_status(torch.zeros(256, dtype=torch.uint8))
+
+
+def _declared_arities():
+    """Parameter count of every PA_API prototype in include/paged_attn.h."""
+    with open(os.path.join(ROOT, "include", "paged_attn.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"PA_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_the_header(lib):
+    # a parameter added on one side only would shift every later argument
+    arities = _declared_arities()
+    assert set(arities) == set(_declared_functions())
+    for name, n in arities.items():
+        fn = getattr(lib._lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
