@@ -234,22 +234,45 @@ def test_binding_rejects_mismatched_varlen_tensors(lib):
         lib.pa_read_device_status(torch.zeros(256, dtype=torch.uint8))
 
 
-def _declared_arities():
-    """Parameter count of every PA_API prototype in include/paged_attn.h."""
+def _declared_params():
+    """Parameter kinds of every PA_API prototype in include/paged_attn.h:
+    'ptr' (any pointer or the stream handle), 'int', 'float', 'size_t'."""
     with open(os.path.join(ROOT, "include", "paged_attn.h")) as f:
         text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
     out = {}
     for m in re.finditer(r"PA_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)\s*;", text):
         params = m.group(2).strip()
-        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+        kinds = []
+        for p in ([] if params in ("", "void") else params.split(",")):
+            if "*" in p or "pa_stream_t" in p:
+                kinds.append("ptr")
+            elif "size_t" in p:
+                kinds.append("size_t")
+            elif "float" in p:
+                kinds.append("float")
+            else:
+                kinds.append("int")
+        out[m.group(1)] = kinds
     return out
 
 
 def test_binding_argtypes_match_the_header(lib):
-    # a parameter added on one side only would shift every later argument
-    arities = _declared_arities()
-    assert set(arities) == set(_declared_functions())
-    for name, n in arities.items():
+    # a parameter added, dropped or retyped on one side only would shift or
+    # reinterpret every later argument
+    decl = _declared_params()
+    assert set(decl) == set(_declared_functions())
+    for name, kinds in decl.items():
         fn = getattr(lib._lib, name)
         assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
-        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        assert len(fn.argtypes) == len(kinds), (name, len(fn.argtypes), len(kinds))
+        for i, (t, k) in enumerate(zip(fn.argtypes, kinds)):
+            if k == "ptr":
+                ok = t is ctypes.c_void_p or t is ctypes.c_char_p or hasattr(t, "_type_") and \
+                    issubclass(t, ctypes._Pointer)
+            elif k == "size_t":
+                ok = t is ctypes.c_size_t
+            elif k == "float":
+                ok = t is ctypes.c_float
+            else:
+                ok = t is ctypes.c_int
+            assert ok, (name, i, t, k)
