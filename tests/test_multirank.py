@@ -89,3 +89,27 @@ def test_two_rank_whole_job_figures():
 def test_single_rank_passthrough():
     bench = _load_bench()
     assert bench.whole_job(5.0, 1e-3, 2e-3, 1, None) == (5.0, 1e-3, 2e-3)
+
+
+def test_reference_arm_line_keeps_the_contract(capsys):
+    # rank 0 of the reference arm: the oracle timed on the host cores, one
+    # JSON line with the bench's keys, its own cpu_baseline and an e2e with
+    # no device copies
+    import argparse
+    import json
+    bench = _load_bench()
+    bench.run_reference(argparse.Namespace(workload="tiny_gqa_decode", seed=3, block_size=16,
+                                           steps=1, warmup=1, gpus=1))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "gpu_launches"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["gpu_launches"] == 0
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny_gqa_decode"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
