@@ -225,6 +225,34 @@ def ncu_traffic(kernel_key: str, src_file: str, workload: str):
     return None
 
 
+def step_time_stats(ms) -> dict:
+    """Summary of per-step times (ms), with every step's time so that an
+    outlier step can be traced to its position in the run."""
+    ms = np.asarray(ms, dtype=np.float64)
+    return {"min_ms": float(ms.min()), "median_ms": float(np.median(ms)),
+            "p90_ms": float(np.percentile(ms, 90)), "max_ms": float(ms.max()),
+            "mean_ms": float(ms.mean()), "per_step_ms": [round(float(x), 5) for x in ms]}
+
+
+def bench_config(case, args, world: int, *, host: bool, step_stats=None) -> dict:
+    """The `config` of both arms, from one place and with the same keys: the
+    workload's shape, the split policy, what one step is, and the timing
+    fields (marked for the host-timed oracle arm)."""
+    splits = getattr(args, "splits", 0)
+    return dict(
+        W.describe(case), splits=splits or "auto",
+        step=("cross-attention over the static encoder cache" if case.cross
+              else "reshape_and_cache + paged attention"),
+        parallelism="single GPU" if world <= 1 else f"replicas x{world}",
+        l2=("n/a (host)" if host else
+            f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB read sweep)"),
+        timing=("host perf_counter around each oracle step" if host else
+                "CUDA events around each step on the launching stream; the host enqueues all "
+                "timed steps while a blocking kernel holds the GPU, so no host launch gap "
+                "falls inside a step"),
+        step_time_stats=step_stats)
+
+
 # ---------------------------------------------------------------- CPU arms
 def oracle_sample_rows(case, target_s: float, threads: int):
     """Pick a prefix of query rows whose oracle run takes about target_s."""
@@ -296,10 +324,10 @@ def run_reference(args):
     kvb = sample_kv_bytes(case, rows)
     for _ in range(args.warmup):
         run_oracle_timed(case, rows, kc, vc, threads)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        run_oracle_timed(case, rows, kc, vc, threads)
-    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    times = np.array([run_oracle_timed(case, rows, kc, vc, threads)
+                      for _ in range(max(1, args.steps))])
+    dt = float(times.mean())
+    step_stats = step_time_stats(times * 1e3)
     value = kvb / dt / 1e9
     sample = (f"{len(rows)} of {case.total_query_tokens} query rows of {case.name} per step "
               f"(all heads), fp64 OpenMP C oracle")
@@ -307,7 +335,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(W.describe(case), l2="n/a (host)", parallelism="rank 0 only"),
+            "config": bench_config(case, args, world, host=True, step_stats=step_stats),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -383,9 +411,19 @@ class Step:
         return self.out
 
 
+def hold_gpu(torch, seconds: float) -> None:
+    """Enqueue a kernel that keeps the GPU busy for about `seconds`, so that
+    the host can enqueue the timed steps behind it and the device never
+    waits for the host inside a step (the blocking-kernel method of
+    GPU benchmark harnesses).  The kernel spins on the SM clock for a fixed
+    count, so it always ends."""
+    torch.cuda._sleep(int(max(seconds, 1e-4) * 2.5e9))
+
+
 def time_steps(step, steps, warmup, flush, e2e=False):
     """Per-step CUDA-event times (ms) of the step and of its attention kernels;
-    L2 is flushed before every timed step, outside the timed interval."""
+    L2 is flushed before every timed step, outside the timed interval.  The
+    host enqueues all timed steps while a blocking kernel holds the GPU."""
     torch = step.torch
     stream = torch.cuda.current_stream()
     host_pack = dev_pack = dev_bufs = None
@@ -417,13 +455,19 @@ def time_steps(step, steps, warmup, flush, e2e=False):
         else:
             step.run(None, prof)
 
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
     for _ in range(warmup):
+        flush.sum()
         one()
+    host_per_step = (time.perf_counter() - h0) / max(1, warmup)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
+    hold_s = min(0.5, 2.0 * steps * host_per_step + 2e-3)
     step.launches = 0
+    hold_gpu(torch, hold_s)
     for i in range(steps):
         flush.sum()  # read-only sweep: evicts L2 without leaving dirty lines behind
         e0, e1, _, _ = ev[i]
@@ -435,6 +479,7 @@ def time_steps(step, steps, warmup, flush, e2e=False):
     # second pass: the attention kernels alone, bracketed by events the
     # library records around them (kept out of the step timing above, where
     # extra events would sit between the chained launches)
+    hold_gpu(torch, hold_s)
     for i in range(steps):
         flush.sum()
         _, _, k0, k1 = ev[i]
@@ -445,7 +490,84 @@ def time_steps(step, steps, warmup, flush, e2e=False):
     kt = np.array([c.elapsed_time(d) for _, _, c, d in ev])
     h2d = sum(v.numel() * v.element_size() for v in step.inputs.values()) if e2e else 0
     d2h = step.out.numel() * step.out.element_size() if e2e else 0
+    if e2e:
+        # the two copies alone (same buffers, same stream), so the step's
+        # end-to-end cost can be split into link time and the rest
+        cev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        hold_gpu(torch, min(0.5, steps * 2e-4 + 2e-3))
+        for e in cev:
+            e[0].record(stream)
+            dev_pack.copy_(host_pack, non_blocking=True)
+            e[1].record(stream)
+            e[2].record(stream)
+            out_host.copy_(step.out, non_blocking=True)
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        h2d_ms = float(np.median([e[0].elapsed_time(e[1]) for e in cev]))
+        d2h_ms = float(np.median([e[2].elapsed_time(e[3]) for e in cev]))
+        time_steps.copy_only = {
+            "h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
+            "h2d_gbs": dev_pack.numel() / (h2d_ms / 1e3) / 1e9,
+            "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9,
+            "note": "median over steps of each copy alone (pinned host memory, one "
+                    "cudaMemcpyAsync each), CUDA events on the step's stream"}
     return t, kt, h2d, d2h
+
+
+def decode_roofline(case, kern_s: float) -> dict:
+    """HBM roofline of decode_kernel: the algorithmic KV bytes (each context
+    token's K and V rows once per KV head) over the kernel's live duration."""
+    kvb = case.kv_bytes()
+    peak, peak_src = measured_hbm_peak()
+    achieved = kvb / kern_s / 1e9
+    traffic = ncu_traffic("decode_kernel", "decode.cu", case.name)
+    return {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
+            "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+            "frac": achieved / peak, "kernel_ms": kern_s * 1e3,
+            "algorithmic_bytes": kvb, "traffic": traffic,
+            "traffic_ratio": (traffic / kvb) if traffic else None}
+
+
+def measure_decode(case, device, splits: int, steps: int, warmup: int, flush) -> dict:
+    """One decode configuration: step time (cache write + attention call),
+    the decode kernel's live time and its HBM roofline."""
+    st = Step(case, device, splits)
+    t, kt, _, _ = time_steps(st, steps, warmup, flush)
+    del st
+    ms = float(t.mean())
+    return {"kv_bytes": case.kv_bytes(), "ms_per_step": ms,
+            "step_gbs": case.kv_bytes() / (ms / 1e3) / 1e9,
+            "tokens_per_s": case.total_query_tokens / (ms / 1e3),
+            "step_time_stats": step_time_stats(t),
+            "roofline": decode_roofline(case, float(kt.mean()) / 1e3),
+            "splits": splits or "auto"}
+
+
+def measure_other_decode_configs(seed: int, device, steps: int, warmup: int, flush) -> dict:
+    """The other decode configurations of the benchmark, each with its own
+    roofline: the tiny GQA decode (a latency figure), the MQA / GQA / MHA
+    sweep at 32 query heads (side by side: KV bytes, tokens/s, kernel
+    fraction of HBM peak, recorded DRAM traffic), and long-context split-KV
+    decode with automatic and fixed split counts."""
+    res = {}
+    tiny = W.tiny_gqa_decode(seed)
+    r = measure_decode(tiny, device, 0, steps, warmup, flush)
+    r["latency_us"] = r["ms_per_step"] * 1e3
+    r["note"] = ("latency-bound: 0.3 MB of KV; the roofline fraction is reported for "
+                 "completeness, the step latency is the figure")
+    res["tiny_gqa_decode"] = r
+    sweep = {}
+    for hkv in (1, 8, 32):
+        c = W.head_sweep(seed, num_kv_heads=hkv)
+        sweep[f"kv{hkv}"] = dict(measure_decode(c, device, 0, steps, warmup, flush),
+                                 num_kv_heads=hkv, G=c.num_heads // hkv)
+        del c
+    res["head_sweep"] = sweep
+    lc = W.long_context_decode(seed)
+    res["long_context_decode"] = {
+        ("auto" if s == 0 else str(s)): measure_decode(lc, device, s, steps, warmup, flush)
+        for s in (0, 16, 32, 64)}
+    return res
 
 
 def prefill_roofline(workload: str, seed: int, device, args, flush):
@@ -497,11 +619,13 @@ def measure_varlen(seed: int, device, steps: int, warmup: int, flush):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    hold_gpu(torch, min(0.5, steps * 4e-4 + 2e-3))
     for e in ev:
         flush.sum()
         e[0].record(stream)
         call()
         e[1].record(stream)
+    hold_gpu(torch, min(0.5, steps * 4e-4 + 2e-3))
     for e in ev:
         flush.sum()
         call((e[2], e[3]))
@@ -591,6 +715,7 @@ def measure_two_kernel(seed: int, device, steps: int, warmup: int, flush, block_
             fn()
         torch.cuda.synchronize()
         ev = []
+        hold_gpu(torch, min(0.5, steps * 6e-4 + 2e-3))
         for _ in range(steps):
             flush.sum()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -639,11 +764,10 @@ def run_ours(args):
     clocks = clk.stop()
     launches = step.launches
 
-    te, _, h2d, d2h = time_steps(step, max(3, args.steps // 2), 2, flush, e2e=True)
+    te, _, h2d, d2h = time_steps(step, max(3, args.steps // 2), max(3, args.warmup), flush,
+                                 e2e=True)
+    del step
 
-    step_stats = {"min_ms": float(t.min()), "median_ms": float(np.median(t)),
-                  "p90_ms": float(np.percentile(t, 90)), "max_ms": float(t.max()),
-                  "mean_ms": float(t.mean())}
     kern_s = float(kt.mean()) / 1e3
     kvb = case.kv_bytes()
     job_kvb, step_s, e2e_s = whole_job(float(kvb), float(t.mean()) / 1e3, float(te.mean()) / 1e3,
@@ -651,14 +775,9 @@ def run_ours(args):
     job_tokens, _, _ = whole_job(float(case.total_query_tokens), 0.0, 0.0, world, device)
     units = "GB/s"
     value = job_kvb / step_s / 1e9
-    peak, peak_src = measured_hbm_peak()
-    achieved = kvb / kern_s / 1e9
+    peak, _ = measured_hbm_peak()
     if case.is_decode:  # also cross-attention decode: the same decode kernel
-        traffic = ncu_traffic("decode_kernel", "decode.cu", case.name)
-        roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
-                    "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                    "frac": achieved / peak, "kernel_ms": kern_s * 1e3,
-                    "algorithmic_bytes": kvb, "traffic": traffic}
+        roofline = decode_roofline(case, kern_s)
     elif case.cross:  # every sequence carries a chunk: the call is the prefill kernel
         flops = prefill_flops(case)
         bpeak, bsrc = measured_bf16_peak()
@@ -676,22 +795,20 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if case.dtype == W.BF16 else "f16", "data": "synthetic",
-        "config": dict(W.describe(case), splits=args.splits or "auto",
-                       l2=f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB read sweep)",
-                       parallelism="replicas" if world > 1 else "single GPU",
-                       step=("cross-attention over the static encoder cache" if case.cross
-                             else "reshape_and_cache + paged attention"),
-                       step_time_stats=step_stats),
+        "config": bench_config(case, args, world, host=False, step_stats=step_time_stats(t)),
         "hbm_peak_frac": value / world / peak,
         "tokens_per_s": job_tokens / step_s,
         "roofline": roofline,
         "e2e": {"value": job_kvb / e2e_s / 1e9, "unit": units, "ms_per_step": e2e_s * 1e3,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "step_time_stats": step_time_stats(te),
+                "copies_alone": getattr(time_steps, "copy_only", None)},
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
 
+    sec_steps, sec_warm = max(10, args.steps), max(3, args.warmup)
     if not args.no_secondary and args.workload == "llama8b_decode":
         mcase = W.mixed_prefill_decode(args.seed + rank, block_size=args.block_size)
         mstep = Step(mcase, device, args.splits)
@@ -708,6 +825,8 @@ def run_ours(args):
             args.seed + rank, device, max(5, args.steps // 2), 3, flush, args.block_size)
         line["secondary"]["varlen_prefill_llama8b"] = measure_varlen(
             args.seed + rank, device, max(5, args.steps // 2), 3, flush)
+        line["secondary"].update(measure_other_decode_configs(
+            args.seed + rank, device, sec_steps, sec_warm, flush))
 
     if rank == 0 and not args.no_cpu_baseline:
         try:

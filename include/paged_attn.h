@@ -265,9 +265,12 @@ PA_API int pa_read_device_status(const void* workspace, int clear, uint32_t* fla
  * Limits and rules:
  *  - a problem whose paged_attn_workspace_bytes() exceeds 32 MiB returns
  *    PA_ERR_WORKSPACE (pass a smaller num_splits, or split the batch);
- *  - the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture;
+ *  - every call made outside a stream capture looks up the array's device
+ *    address (cudaGetSymbolAddress) with the current device, so a context
+ *    that was reset and created again is followed; a call inside a capture
+ *    reuses the address of the device's latest uncaptured call, so make the
+ *    first call on each device before any stream capture (a first call
+ *    inside a capture returns PA_ERR_CUDA);
  *  - all calls share the one array and each call's work-list kernel
  *    rewrites what the next kernels read, so nothing needs clearing, but
  *    calls that overlap on the GPU (other streams, other host threads) race

@@ -33,16 +33,25 @@ std::mutex g_scratch_mu;
 
 // Device address of the array on the current device.  Host code only sees a
 // host-side stand-in for `g_decode_scratch`; the real address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
-int scratch_address(void** out) {
+// cudaGetSymbolAddress with that device current.  It is looked up again on
+// every call made outside a stream capture (a cheap host-side query), since
+// a context torn down and created again (cudaDeviceReset) loads the module
+// anew and the array may then sit elsewhere.  Inside a capture the address
+// of the device's latest uncaptured call is used, so the first call on a
+// device must come before any capture.
+int scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices)
     return PA_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
     g_scratch_addr[dev] = p;
+  } else if (!g_scratch_addr[dev]) {
+    return PA_ERR_CUDA;  // first call on this device inside a capture
   }
   *out = g_scratch_addr[dev];
   return PA_OK;
@@ -67,7 +76,7 @@ PA_API int paged_attn_decode_noalloc(const void* q, const void* k_cache, const v
                              context_lens, scale, num_seqs, num_heads, num_kv_heads, head_dim,
                              block_size, num_blocks, dtype, num_splits, out, nullptr, 0, stream);
   void* ws = nullptr;
-  const int rc = pa::scratch_address(&ws);
+  const int rc = pa::scratch_address(reinterpret_cast<cudaStream_t>(stream), &ws);
   if (rc != PA_OK) return rc;
   // The work-list kernel rewrites every counter and list the decode kernels
   // read, so the contents left by the previous call need no clearing.
