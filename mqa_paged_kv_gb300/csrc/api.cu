@@ -184,6 +184,9 @@ int check_common(const void* q, const void* k_cache, const void* v_cache,
 
 WsLayout decode_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                        int max_blocks_per_seq, int block_size, int num_splits) {
+  if (num_heads % num_kv_heads == 0 &&
+      use_equal_share(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, num_splits))
+    return equal_share_layout(num_seqs, num_heads, num_kv_heads, head_dim);
   const int64_t pairs =
       static_cast<int64_t>(num_seqs) * max_splits_per_seq(max_blocks_per_seq, block_size, num_splits);
   (void)num_kv_heads;
@@ -298,6 +301,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   pp.total_tokens = total_query_tokens;
   pp.causal = causal;
   pp.cu_key_lens = nullptr;
+  pp.header_only = 0;
   // A batch with query chunks runs its prefill and decode kernels side by
   // side; the work-list kernel splits the grid between them.
   const bool concurrent = max_query_len > 1;
@@ -339,6 +343,12 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   dp.scale_log2 = fp.scale_log2;
   dp.trigger_dependents = num_splits != 1;
   dp.concurrent = concurrent ? 1 : 0;
+  dp.part_row_stride = num_heads;
+  dp.part_kvh_rows = G;
+  dp.equal_share = 0;
+  dp.context_lens = context_lens;
+  dp.num_seqs = num_seqs;
+  dp.sk_prefix = nullptr;
 
   const ProfileScope prof(st);
   int n = 0, r;
@@ -367,6 +377,9 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
     cp.num_seqs = num_seqs;
     cp.num_heads = num_heads;
     cp.head_dim = head_dim;
+    cp.sk_prefix = nullptr;
+    cp.num_kv_heads = num_kv_heads;
+    cp.sk_groups = 0;
     if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
     n += r;
   }
@@ -491,6 +504,10 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   pp.causal = 1;
   pp.cu_key_lens = nullptr;
   pp.split_ctas = 0;
+  pp.header_only = L.equal_share ? 1 : 0;
+  // Equal shares: the grid (one CTA per SM) fixes the groups' tile ranges.
+  int grid = grid_sms(dev, cta_limit);
+  if (L.equal_share && grid > kSkMaxCtas) grid = kSkMaxCtas;
 
   DecodeParams dp;
   dp.q = q;
@@ -509,15 +526,19 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   dp.scale_log2 = scale * 1.4426950408889634f;
   dp.trigger_dependents = num_splits != 1;
   dp.concurrent = 0;
-
+  dp.equal_share = L.equal_share ? 1 : 0;
+  dp.part_row_stride = L.equal_share ? G : num_heads;
+  dp.part_kvh_rows = L.equal_share ? 0 : G;
+  dp.context_lens = context_lens;
+  dp.num_seqs = num_seqs;
+  dp.sk_prefix = reinterpret_cast<int32_t*>(ws + L.seq_info);
 
   const ProfileScope prof(st);
   int n = 0, r;
   if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
   n += r;
   prof.begin();
-  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, grid_sms(dev, cta_limit))) < 0)
-    return cuda_error();
+  if ((r = launch_decode(tmk, tmv, dp, bf16, head_dim, st, grid)) < 0) return cuda_error();
   n += r;
   prof.end();
   if (num_splits != 1) {
@@ -529,7 +550,12 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
     cp.num_seqs = num_seqs;
     cp.num_heads = num_heads;
     cp.head_dim = head_dim;
-    if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
+    cp.sk_prefix = dp.sk_prefix;
+    cp.num_kv_heads = num_kv_heads;
+    cp.sk_groups = grid * decode_groups_per_cta(G);
+    r = L.equal_share ? launch_combine_equal_share(cp, bf16, head_dim, st)
+                      : launch_combine(cp, bf16, head_dim, st);
+    if (r < 0) return cuda_error();
     n += r;
   }
   return finish(n);

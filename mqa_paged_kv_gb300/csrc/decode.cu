@@ -72,7 +72,8 @@ struct DecodeSmem {
   static constexpr int kBarsPerGroup = 2 * R + (kHM ? 2 : 0);  // full, empty, query slots
   static constexpr int kBars = kGroups * kBarsPerGroup * 8;
   static constexpr int kMeta = kGroups * R * static_cast<int>(sizeof(StageMeta));
-  static constexpr int kBytes = kRing + kQSlots + kBars + kMeta + 1024;  // + alignment slack
+  static constexpr int kUsed = kRing + kQSlots + kBars + kMeta;  // then the equal-share arrays
+  static constexpr int kBytes = kUsed + 1024;  // + alignment slack
 };
 
 // Producer-side description of the item whose tiles are being issued.
@@ -145,18 +146,75 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
   fence_proxy_async();
   __syncthreads();
-  // The work list is written by the work-list kernel.  Normally that is the
-  // preceding kernel and this one waits for it; beside a prefill kernel
-  // this one starts without a wait (the prefill kernel let it start only
-  // after its own wait for the list) and reads the list through L2.
-  if (!p.concurrent) griddep_wait();
-  if (p.trigger_dependents) griddep_launch_dependents();  // the split combine may become resident
 
-  const uint32_t num_items = p.concurrent ? __ldcg(&p.hdr->decode_items) : p.hdr->decode_items;
   const int G = p.G, Hq = p.num_heads, Hkv = p.num_kv_heads, bs = p.block_size;
   const bool producer = kHM ? (wig == GS) : (wig == 0);
   uint32_t* status = &p.hdr->status;
   const uint16_t* qg = static_cast<const uint16_t*>(p.q);
+
+  // ------------------------------------------------ equal share: prologue
+  // Every CTA scans the lengths into a prefix of key tiles per sequence,
+  // n_b = ceil(ctx_b / 16) (unit (b, kvh) owns tiles Hkv * P[b] + kvh * n_b
+  // onward), and each warp group takes the tile range
+  // [g * T / NG, (g + 1) * T / NG) of the T = Hkv * P[B] tiles (integer
+  // shares, the first T mod NG groups one tile more).  Lengths and block
+  // tables are final before this kernel can start, so all of it runs before
+  // the wait for the preceding kernels.
+  int32_t* skP = reinterpret_cast<int32_t*>(smem + S::kUsed);  // [B + 1]
+  int32_t* skC = skP + p.num_seqs + 1;                         // [B] lengths
+  int sk_t = 0, sk_end = 0, sk_gstart = 0, sk_gg = 0;
+  bool sk_bad = false;
+  if (p.equal_share) {
+    int32_t* wsum = skC + p.num_seqs;
+    const int nwarps = blockDim.x >> 5;
+    const int max_ctx = p.mbs * bs;
+    int carry = 0;
+    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+      const int b = base + threadIdx.x;
+      int n = 0;
+      if (b < p.num_seqs) {
+        int c = __ldg(p.context_lens + b);
+        if (c < 0 || c > max_ctx) {  // outside the contract: no keys, flagged
+          sk_bad = true;
+          c = 0;
+        }
+        skC[b] = c;
+        n = (c + kKeyTile - 1) / kKeyTile;
+      }
+      int x = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (lane == 31) wsum[warp] = x;
+      __syncthreads();
+      if (warp == 0) {
+        int w = lane < nwarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, w, off);
+          if (lane >= off) w += y;
+        }
+        if (lane < nwarps) wsum[lane] = w;
+      }
+      __syncthreads();
+      if (b < p.num_seqs) skP[b] = carry + (warp ? wsum[warp - 1] : 0) + x - n;
+      carry += wsum[nwarps - 1];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) skP[p.num_seqs] = carry;
+    sk_bad = __syncthreads_or(sk_bad) != 0;
+    const int total = Hkv * carry;
+    const int ng = static_cast<int>(gridDim.x) * S::kGroups;
+    sk_gg = static_cast<int>(blockIdx.x) * S::kGroups + group;
+    const int q = total / ng, r = total - q * ng;
+    sk_gstart = sk_gg * q + min(sk_gg, r);
+    sk_end = sk_gstart + q + (sk_gg < r ? 1 : 0);
+    sk_t = sk_gstart;
+  }
+  const uint32_t num_items =
+      p.equal_share ? 0u : (p.concurrent ? __ldcg(&p.hdr->decode_items) : p.hdr->decode_items);
 
   // ---------------------------------------------------------------- producer
   uint32_t p_iter = 0;
@@ -181,6 +239,35 @@ __global__ void __launch_bounds__(NW * 32, 1)
   };
 
   auto advance = [&]() {
+    if (nx.state == 0 && p.equal_share) {
+      // The next piece of this group's range: the unit holding tile sk_t
+      // (the last sequence whose first tile is at or before it; empty
+      // sequences share their successor's prefix), cut at the range's end.
+      if (sk_t >= sk_end) {
+        nx.state = 4;
+        return;
+      }
+      int lo = 0, hi = p.num_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (Hkv * skP[mid] <= sk_t) lo = mid; else hi = mid - 1;
+      }
+      const int base = Hkv * skP[lo], n = skP[lo + 1] - skP[lo];
+      const int kvh = (sk_t - base) / n;
+      const int su = base + kvh * n, eu = su + n;
+      const int pe = min(sk_end, eu);
+      nx.kvh = kvh;
+      nx.rec.b = lo;
+      nx.rec.tok = lo;
+      nx.rec.key_begin = (sk_t - su) * kKeyTile;
+      nx.rec.key_end = pe == eu ? skC[lo] : (pe - su) * kKeyTile;
+      // a whole unit writes its output row; a cut one its partial, in the
+      // group's first slot when it opens the range, else in the second
+      nx.rec.part_idx = (sk_t == su && pe == eu) ? -1 : 2 * sk_gg + (sk_t == sk_gstart ? 0 : 1);
+      sk_t = pe;
+      nx.state = 2;
+      return;
+    }
     if (nx.state == 0) {
       uint32_t it = 0;
       if (lane == 0) it = atomicAdd(&p.hdr->decode_grab, 1u);
@@ -301,6 +388,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
     ++p_iter;
     if (nx.state < 3) advance();
   };
+
+  // Wait for the preceding kernels (the cache write; the work-list kernel,
+  // which writes the sorted list and resets the status word).  With equal
+  // shares each producer first prepares its first piece (record and block
+  // ids).  Beside a prefill kernel this kernel starts without a wait (the
+  // prefill kernel let it start only after its own wait for the list) and
+  // reads the list through L2.
+  if (p.equal_share) {
+    if (producer)
+      while (nx.state < 3) advance();
+    griddep_wait();
+    if (blockIdx.x == 0) {  // the tile prefix, for the combine
+      for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) p.sk_prefix[i] = skP[i];
+      if (threadIdx.x == 0 && sk_bad) Status::raise(status, PA_DEV_BAD_LENGTHS);
+    }
+  } else if (!p.concurrent) {
+    griddep_wait();
+  }
+  if (p.trigger_dependents) griddep_launch_dependents();  // the split combine may become resident
 
   const int g = lane >> 2, q4 = lane & 3;   // MMA fragment: row group, column pair
   const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: matrix index, row in it
@@ -470,8 +576,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
                   pack2<kBF16>(o[nt][2] * il1, o[nt][3] * il1);
           }
         } else {
-          float* po = p.part_o +
-                      (static_cast<int64_t>(m.part_idx) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+          const int64_t prow = static_cast<int64_t>(m.part_idx) * p.part_row_stride +
+                               static_cast<int64_t>(m.kvh) * p.part_kvh_rows;
+          float* po = p.part_o + prow * D;
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             const int d = nt * 8 + 2 * q4;
@@ -483,8 +590,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                   make_float2(o[nt][2] * il1, o[nt][3] * il1);
           }
           if (q4 == 0) {
-            float* pl = p.part_lse + static_cast<int64_t>(m.part_idx) * Hq +
-                        static_cast<int64_t>(m.kvh) * G;
+            float* pl = p.part_lse + prow;
             if (h0 < G) pl[h0] = l0 > 0.f ? mref[0] + __log2f(l0) : -INFINITY;
             if (h1 < G) pl[h1] = l1 > 0.f ? mref[1] + __log2f(l1) : -INFINITY;
           }
@@ -531,8 +637,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
           }
         }
       } else {
-        float* po = p.part_o +
-                    (static_cast<int64_t>(m.part_idx) * Hq + static_cast<int64_t>(m.kvh) * G) * D;
+        const int64_t prow = static_cast<int64_t>(m.part_idx) * p.part_row_stride +
+                             static_cast<int64_t>(m.kvh) * p.part_kvh_rows;
+        float* po = p.part_o + prow * D;
         const int h0 = hb + 2 * q4, h1 = h0 + 1;
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt) {
@@ -547,8 +654,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
           }
         }
         if (g == 0) {
-          float* pl = p.part_lse + static_cast<int64_t>(m.part_idx) * Hq +
-                      static_cast<int64_t>(m.kvh) * G;
+          float* pl = p.part_lse + prow;
           if (h0 < G) pl[h0] = l0 > 0.f ? mrow[0] + __log2f(l0) : -INFINITY;
           if (h1 < G) pl[h1] = l1 > 0.f ? mrow[1] + __log2f(l1) : -INFINITY;
         }
@@ -773,6 +879,107 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_kernel(const Combi
   }
 }
 
+// Merge of the equal-share partials.  Unit u = (b, kvh) owns tiles
+// [S_u, E_u) and group g the range [start(g), start(g + 1)); the unit was
+// cut when its first and last tiles lie in different groups, g_f and g_l.
+// Each group g in [g_f, g_l] wrote the unit's piece to its first slot (2g)
+// when its range opens inside the unit, and to its second (2g + 1) when
+// the unit opens inside its range, which only g_f's can.  Per head (one
+// warp): M = max_g lse_g, out = sum_g 2^(lse_g - M) o_g / sum_g 2^(lse_g - M),
+// lse in base 2.  Units that were not cut were written by the decode
+// kernel; sequences without keys get zero rows here.
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(32 * kCombineHeads) combine_equal_share_kernel(
+    const CombineParams p) {
+  griddep_wait();  // partials and the tile prefix are written by the decode kernel
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kCombineHeads + warp;
+  const int Hq = p.num_heads, Hkv = p.num_kv_heads, G = Hq / Hkv;
+  if (h >= Hq) return;
+  constexpr int kV = D / 32;  // values per lane
+  uint16_t* dst = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(b) * Hq + h) * D + lane * kV;
+  auto store = [&](const float (&v)[kV]) {
+    uint32_t packed[kV / 2];
+#pragma unroll
+    for (int i = 0; i < kV / 2; ++i) packed[i] = pack2<kBF16>(v[2 * i], v[2 * i + 1]);
+    if constexpr (kV == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    }
+  };
+  const int pb = __ldcg(p.sk_prefix + b), n = __ldcg(p.sk_prefix + b + 1) - pb;
+  if (n == 0) {  // no keys: a zero row
+    float z[kV];
+#pragma unroll
+    for (int i = 0; i < kV; ++i) z[i] = 0.f;
+    store(z);
+    return;
+  }
+  const int total = Hkv * __ldcg(p.sk_prefix + p.num_seqs);
+  const int ng = p.sk_groups, q = total / ng, r = total - q * ng;
+  const int kvh = h / G, hg = h - kvh * G;
+  const int su = Hkv * pb + kvh * n, eu = su + n;
+  auto group_of = [&](int t) {
+    return t < r * (q + 1) ? t / (q + 1) : r + (t - r * (q + 1)) / q;
+  };
+  const int gf = group_of(su), gl = group_of(eu - 1);
+  if (gf == gl) return;  // one piece: written by the decode kernel
+  const bool f_second = gf * q + min(gf, r) < su;
+  const int np = gl - gf + 1;
+  auto slot_row = [&](int i) {  // partial row of piece i (group gf + i)
+    const int gg = gf + i;
+    return static_cast<int64_t>(2 * gg + (i == 0 && f_second ? 1 : 0)) * G + hg;
+  };
+  float M = -INFINITY;
+  for (int c = lane; c < np; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot_row(c)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[kV], W = 0.f;
+#pragma unroll
+  for (int i = 0; i < kV; ++i) acc[i] = 0.f;
+  for (int c0 = 0; c0 < np; c0 += 32) {
+    const float l = c0 + lane < np ? __ldcg(p.part_lse + slot_row(c0 + lane)) : -INFINITY;
+    const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : ex2(l - M);
+    W += w;
+    const int cnt = min(32, np - c0);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float v[8][kV];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < cnt) {
+          const float* src = p.part_o + slot_row(c0 + j0 + j) * D + lane * kV;
+          if constexpr (kV == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            v[j][0] = t.x; v[j][1] = t.y;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+        if (j0 + j < cnt) {
+#pragma unroll
+          for (int i = 0; i < kV; ++i) acc[i] += wj * v[j][i];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+  for (int i = 0; i < kV; ++i) acc[i] *= inv;
+  store(acc);
+}
+
 // ---------------------------------------------------------------- launchers
 namespace {
 
@@ -789,13 +996,16 @@ int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
   constexpr int R = kR0 < 2 ? 2 : (kR0 > 8 ? 8 : kR0);
   using S = DecodeSmem<D, GS, NW, R, kHM>;
   static_assert(S::kGroups == kGroups, "warps split into whole groups");
-  static_assert(S::kBytes <= 227 * 1024, "fits one CTA per SM");
+  static_assert(kGroups == decode_groups_per_cta(kHM ? (GS == 1 ? 16 : 16 * GS) : 8),
+                "the host's group count matches the launched configuration");
+  constexpr int kMaxBytes = S::kBytes + static_cast<int>(sk_smem_bytes(kSkMaxSeqs));
+  static_assert(kMaxBytes <= 227 * 1024, "fits one CTA per SM");
   auto kern = decode_kernel<kBF16, D, GS, NW, R, kHM>;
   static int configured = -1;  // device whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured != dev) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBytes) !=
         cudaSuccess)
       return -1;
     configured = dev;
@@ -803,7 +1013,8 @@ int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(NW * 32);
-  cfg.dynamicSmemBytes = S::kBytes;
+  cfg.dynamicSmemBytes =
+      S::kBytes + (p.equal_share ? static_cast<int>(sk_smem_bytes(p.num_seqs)) : 0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -846,6 +1057,30 @@ int launch_combine(const CombineParams& p, bool bf16, int head_dim, cudaStream_t
   else
     e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_kernel<false, 64>, p)
                        : cudaLaunchKernelEx(&cfg, combine_kernel<false, 128>, p);
+  return e == cudaSuccess ? 1 : -1;
+}
+
+int launch_combine_equal_share(const CombineParams& p, bool bf16, int head_dim,
+                               cudaStream_t stream) {
+  if (p.num_seqs <= 0) return 0;
+  cudaLaunchConfig_t cfg = {};
+  const int heads = p.num_heads < kCombineHeads ? p.num_heads : kCombineHeads;
+  cfg.gridDim = dim3(p.num_seqs, (p.num_heads + kCombineHeads - 1) / kCombineHeads);
+  cfg.blockDim = dim3(32 * heads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (bf16)
+    e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_equal_share_kernel<true, 64>, p)
+                       : cudaLaunchKernelEx(&cfg, combine_equal_share_kernel<true, 128>, p);
+  else
+    e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, combine_equal_share_kernel<false, 64>, p)
+                       : cudaLaunchKernelEx(&cfg, combine_equal_share_kernel<false, 128>, p);
   return e == cudaSuccess ? 1 : -1;
 }
 

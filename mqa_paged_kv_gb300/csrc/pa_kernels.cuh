@@ -18,6 +18,27 @@ constexpr int kMaxSplits = 64;        // splits per sequence, at most
 constexpr int kPrefillTileRows = 128; // (token, head) rows of one MMA tile
 constexpr int kPrefillKeys = 64;      // keys per prefill pipeline stage
 
+// Equal-share decode (automatic splits of the decode entry point): every
+// warp group of the persistent grid takes an equal contiguous range of the
+// batch's key tiles, units (sequence, KV head) being cut where the ranges
+// end.  The lengths are scanned in each CTA's shared memory, which bounds
+// the batch; the partial slots are sized for a bounded grid.
+constexpr int kSkMaxSeqs = 2048;  // larger batches take the sorted work list
+constexpr int kSkMaxCtas = 160;   // CTAs of an equal-share grid, at most
+
+// Warp groups per decode CTA for G query heads per KV head (the launcher's
+// configurations: swap AB with one warp per group for G <= 8; head major
+// with ceil(G / 16) consumer warps and one producer warp per group above).
+constexpr int decode_groups_per_cta(int G) {
+  return G <= 8 ? 8 : (G <= 16 ? 6 : (G <= 32 ? 4 : 2));
+}
+
+// Shared memory of the equal-share prologue: tile prefix [B + 1], lengths
+// [B] and the scan's warp sums.
+constexpr size_t sk_smem_bytes(int num_seqs) {
+  return (static_cast<size_t>(2 * num_seqs + 1) * 4 + 32 * 4 + 15) / 16 * 16;
+}
+
 // ------------------------------------------------------------------ records
 // Header at the start of every workspace (256 bytes).
 struct WsHeader {
@@ -67,6 +88,7 @@ struct PfTile {
 struct WsLayout {
   size_t seq_info, pairs, part_lse, part_o, tiles, total;
   int64_t max_pairs, max_tiles;
+  bool equal_share;  // the decode call runs the equal-share decomposition
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -105,6 +127,42 @@ inline WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int6
   L.total = off;
   L.max_pairs = max_pairs;
   L.max_tiles = max_tiles;
+  L.equal_share = false;
+  return L;
+}
+
+// Whether a decode call with these sizes uses the equal-share decomposition
+// (host side, from sizes only): automatic splits, a batch whose lengths fit
+// the prologue's shared memory, and tile counts that fit 32-bit indices.
+inline bool use_equal_share(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
+                            int block_size, int num_splits) {
+  if (num_splits != 0 || num_seqs <= 0 || num_seqs > kSkMaxSeqs) return false;
+  const int64_t tiles_per_seq =
+      (static_cast<int64_t>(max_blocks_per_seq) * block_size + kKeyTile - 1) / kKeyTile;
+  return tiles_per_seq * num_seqs * num_kv_heads < (int64_t{1} << 31);
+}
+
+// Equal-share workspace: header, the tile prefix over sequences [B + 1]
+// (written by the decode kernel for the combine), and two partial slots
+// per warp group -- the unit piece at the start of its range and the one
+// at its end -- each holding G rows of D fp32 values and G log-sum-exps.
+inline WsLayout equal_share_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
+  const int G = num_heads / num_kv_heads;
+  const int64_t slots = 2 * static_cast<int64_t>(kSkMaxCtas) * decode_groups_per_cta(G);
+  WsLayout L;
+  size_t off = sizeof(WsHeader);
+  L.seq_info = off;  // the tile prefix
+  off = align_up(off + sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1), 256);
+  L.pairs = off;
+  L.part_lse = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(slots) * G, 256);
+  L.part_o = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(slots) * G * head_dim, 256);
+  L.tiles = off;
+  L.total = off;
+  L.max_pairs = slots;
+  L.max_tiles = 0;
+  L.equal_share = true;
   return L;
 }
 
@@ -125,6 +183,7 @@ struct PrepareParams {
                                // [cu_key_lens[b], cu_key_lens[b+1]); all rows take tiles
   int64_t total_tokens;  // rows of q / out
   int split_ctas;        // > 0: a mixed batch's grid, to be split between decode and prefill
+  int header_only;       // equal-share decode: only reset the status word (no lists)
 };
 
 struct DecodeParams {
@@ -141,6 +200,17 @@ struct DecodeParams {
   // kernel of a mixed batch): only then may the next launch start early (a
   // following call's work-list build must not overlap this kernel).
   int trigger_dependents;
+  // Partial of item part_idx, KV head kvh, head h of the group at row
+  // part_idx * part_row_stride + kvh * part_kvh_rows + h of part_o / part_lse
+  // (sorted list: Hq and G; equal share: G and 0).
+  int part_row_stride, part_kvh_rows;
+  // Equal-share decomposition (1) instead of the sorted work list: the
+  // lengths are read and scanned in the prologue, and CTA 0 stores the tile
+  // prefix at sk_prefix for the combine.
+  int equal_share;
+  const int32_t* context_lens;
+  int num_seqs;
+  int32_t* sk_prefix;
   // 1 in a batch with query chunks: launched after the prefill kernel and
   // beside it, on the SMs its CTAs past the prefill share leave (its other
   // CTAs join as prefill CTAs finish): no wait at the start (the work list
@@ -156,6 +226,9 @@ struct CombineParams {
   const float* part_lse;
   void* out;
   int num_seqs, num_heads, head_dim;
+  // equal share: the tile prefix over sequences and the decode grid's groups
+  const int32_t* sk_prefix;
+  int num_kv_heads, sk_groups;
 };
 
 // A batch with query chunks runs its prefill and decode kernels side by
@@ -201,6 +274,10 @@ int launch_decode(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodePa
                   bool bf16, int head_dim, cudaStream_t stream, int num_sms);
 
 int launch_combine(const CombineParams& p, bool bf16, int head_dim, cudaStream_t stream);
+
+// Merge of the equal-share partials (and zero rows of key-less sequences).
+int launch_combine_equal_share(const CombineParams& p, bool bf16, int head_dim,
+                               cudaStream_t stream);
 
 int launch_prefill_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
                       const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,

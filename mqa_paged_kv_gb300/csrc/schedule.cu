@@ -141,6 +141,13 @@ __device__ __forceinline__ int block_scan(int v, int* warp_sums, int& excl) {
 template <bool kSplit>
 __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   griddep_launch_dependents();  // the attention kernel may start its prologue
+  if (p.header_only) {
+    // Equal-share decode: the decode kernel derives its work from the
+    // lengths itself; only the status word of this call starts at zero.
+    if (threadIdx.x == 0) p.hdr->status = 0;
+    griddep_wait();
+    return;
+  }
   // The lengths this kernel reads are final before the previous kernel
   // could let it start early: a kernel of the caller triggers this launch
   // only when it completes, and the library's own cache write (the one
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
 int launch_prepare(const PrepareParams& p, bool /*bf16*/, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(p.header_only ? 32 : kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -49,8 +49,21 @@ def test_workspace_sizes(lib):
     b = lib.paged_attn_workspace_bytes(256, 32, 8, 128, 256, 16, 1)
     c = lib.paged_attn_workspace_bytes(8, 32, 8, 128, 2048, 16, 0)
     assert a > b > 0 and c > 0
-    # auto splits cap at 64 per sequence: 8 seqs x 64 splits x 32 heads x (128 + 1) floats
-    assert c >= 8 * 64 * 32 * 129 * 4
+    # automatic splits up to 2048 sequences: equal shares of the key tiles,
+    # two partial slots per warp group of a grid of at most 160 CTAs (8
+    # groups of G = 4 heads), each G x (128 + 1) floats, whatever the lengths
+    slots = 2 * 160 * 8
+    assert a >= slots * 4 * 129 * 4 and c >= slots * 4 * 129 * 4
+    assert abs(a - c) < 65536
+    # G = 32 (MQA): 4 groups per CTA of 32 heads each
+    m = lib.paged_attn_workspace_bytes(128, 32, 1, 128, 64, 16, 0)
+    assert m >= 2 * 160 * 4 * 32 * 129 * 4
+    # fixed splits, or past 2048 sequences, the sorted work list: partials of
+    # every (sequence, split), automatic splits capped at 64 per sequence
+    d = lib.paged_attn_workspace_bytes(8, 32, 8, 128, 2048, 16, 64)
+    e = lib.paged_attn_workspace_bytes(2100, 32, 8, 128, 2048, 16, 0)
+    assert d >= 8 * 64 * 32 * 129 * 4
+    assert e >= 2100 * 64 * 32 * 129 * 4
     assert lib.paged_attn_chunked_prefill_workspace_bytes(64, 4434, 32, 8, 128, 256, 16, 0) > 0
 
 

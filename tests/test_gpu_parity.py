@@ -234,12 +234,19 @@ def test_split_count_independence():
 
 
 def test_chunked_entry_with_only_decode_rows_equals_decode_bitwise():
+    # with a fixed split count both entry points run the same sorted work
+    # list; with automatic splits the decode entry point takes equal shares
+    # of the key tiles instead, so there both are held to the oracle
     c = W.llama8b_decode(6, batch=20, max_ctx=2000)
     g = GpuCase(c)
     g.write_cache()
-    a = bits(g.attention())
-    b = bits(g.attention(force_chunked=True))
-    assert np.array_equal(a, b)
+    for s in (1, 3):
+        a = bits(g.attention(num_splits=s))
+        b = bits(g.attention(num_splits=s, force_chunked=True))
+        assert np.array_equal(a, b)
+    o64, ob, _, _ = oracle.run_case(c)
+    check_attention(bits(g.attention()), o64, ob, c.dtype)
+    check_attention(bits(g.attention(force_chunked=True)), o64, ob, c.dtype)
 
 
 def test_gqa_matches_mha_on_duplicated_kv_heads():
@@ -348,9 +355,10 @@ def test_cross_attention_decode_workload():
     # one query row per sequence: the plain decode entry point over the same
     # cache is the same computation
     ref = g.pa.paged_attn_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens,
-                                 c.scale)
+                                 c.scale, num_splits=4)
+    cross = g.attention(num_splits=4)
     torch.cuda.synchronize()
-    assert np.array_equal(bits(ref), bits(out))
+    assert np.array_equal(bits(ref), bits(cross))
 
 
 def test_cross_attention_prefill_workload_sampled_rows():
@@ -425,12 +433,79 @@ def test_cta_limit_gives_the_same_bits(limit):
 # large sizes: batches beyond one work-list pass, long single chunks
 # --------------------------------------------------------------------------
 
-def test_decode_batch_beyond_one_work_list_pass():
+@pytest.mark.parametrize("batch,splits", [(1500, 0), (1500, 2), (2100, 0)])
+def test_decode_batch_beyond_one_work_list_pass(batch, splits):
     # more sequences than the work-list kernel's 512 threads: the multi-pass
-    # path (split offsets read back from the workspace)
-    c = W.llama8b_decode(31, batch=1500, max_ctx=1024)
+    # path (split offsets read back from the workspace) with fixed splits, and
+    # past the equal-share batch limit (2048) with automatic ones; 1500
+    # sequences with automatic splits scan the lengths in several passes of
+    # the decode kernel's prologue
+    c = W.llama8b_decode(31, batch=batch, max_ctx=1024)
     rows = np.sort(np.random.default_rng(3).choice(c.num_seqs, 96, replace=False))
-    run_and_check(c, rows=rows)
+    run_and_check(c, rows=rows, num_splits=splits)
+
+
+# --------------------------------------------------------------------------
+# equal-share decode (automatic splits of the decode entry point)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("limit", [1, 7, 37])
+def test_equal_share_under_cta_limits(limit):
+    # the groups' tile ranges follow the grid: a smaller grid cuts the units
+    # elsewhere (other partials, same result within the tolerance); the same
+    # grid twice gives the same bits
+    c = W.llama8b_decode(41, batch=40, max_ctx=3000)
+    g = GpuCase(c)
+    g.write_cache()
+    o64, ob, _, _ = oracle.run_case(c)
+    g.pa.pa_limit_next_call_ctas(limit)
+    a = bits(g.attention())
+    g.pa.pa_limit_next_call_ctas(limit)
+    b = bits(g.attention())
+    torch.cuda.synchronize()
+    assert np.array_equal(a, b)
+    check_attention(a, o64, ob, c.dtype)
+    assert g.status() == 0
+
+
+def test_equal_share_one_sequence_over_every_group():
+    # one MQA unit of 32k keys cut into a piece per warp group (more pieces
+    # than a warp's 32 lanes in the merge), and one GQA sequence beside a run
+    # of empty ones
+    for hkv, ctx in ((1, [32768]), (8, [0, 0, 0, 20000, 0])):
+        ctx = np.array(ctx)
+        c = W.make_case("one_long", seed=43 + hkv, dtype=W.BF16, num_heads=32,
+                        num_kv_heads=hkv, head_dim=128, block_size=16,
+                        context_lens=np.maximum(ctx, 1), query_lens=np.ones(len(ctx), np.int64))
+        c.context_lens = c.context_lens.copy()
+        c.context_lens[ctx == 0] = 0          # key-less sequences
+        c.slot_mapping = np.where(ctx > 0, c.slot_mapping, -1)  # nothing to write for them
+        g = GpuCase(c)
+        g.write_cache()
+        out = g.attention()
+        torch.cuda.synchronize()
+        got = bits(out)
+        live = np.nonzero(c.context_lens > 0)[0]
+        o64, ob, _, _ = oracle.run_case(c, rows=live)
+        check_attention(got[live], o64, ob, c.dtype)
+        assert not got[c.context_lens == 0].any()  # key-less sequences: zero rows
+
+
+def test_equal_share_bad_length_is_flagged():
+    c = W.llama8b_decode(44, batch=6, max_ctx=500)
+    g = GpuCase(c)
+    g.write_cache()
+    ctx = g.context_lens.clone()
+    ctx[2] = c.max_blocks_per_seq * c.block_size + 1   # beyond the table
+    g.context_lens = ctx
+    out = g.attention()
+    torch.cuda.synchronize()
+    assert g.status() & g.pa.PA_DEV_BAD_LENGTHS
+    got = bits(out)
+    assert not got[2].any()                            # no keys read: a zero row
+    rows = np.array([0, 1, 3, 4, 5])
+    o64, ob, _, _ = oracle.run_case(c, rows=rows)
+    check_attention(got[rows], o64, ob, c.dtype)
 
 
 def test_mixed_batch_beyond_one_work_list_pass():
