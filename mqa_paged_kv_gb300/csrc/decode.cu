@@ -213,8 +213,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     sk_end = sk_gstart + q + (sk_gg < r ? 1 : 0);
     sk_t = sk_gstart;
   }
-  const uint32_t num_items =
-      p.equal_share ? 0u : (p.concurrent ? __ldcg(&p.hdr->decode_items) : p.hdr->decode_items);
+  // Sorted list: its length, read once the list is complete (after the wait
+  // below; the lambdas that use it only run after that point).
+  uint32_t num_items = 0;
 
   // ---------------------------------------------------------------- producer
   uint32_t p_iter = 0;
@@ -403,8 +404,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) p.sk_prefix[i] = skP[i];
       if (threadIdx.x == 0 && sk_bad) Status::raise(status, PA_DEV_BAD_LENGTHS);
     }
-  } else if (!p.concurrent) {
-    griddep_wait();
+  } else {
+    if (!p.concurrent) griddep_wait();
+    num_items = p.concurrent ? __ldcg(&p.hdr->decode_items) : p.hdr->decode_items;
   }
   if (p.trigger_dependents) griddep_launch_dependents();  // the split combine may become resident
 
