@@ -68,8 +68,13 @@ struct DecodeSmem {
   static constexpr int kWarpsPerGroup = kHM ? GS + 1 : GS;
   static constexpr int kGroups = NW / kWarpsPerGroup;
   static constexpr int kRing = kGroups * R * T::kStage;
-  static constexpr int kQSlots = kHM ? kGroups * 2 * T::kQ : 0;
-  static constexpr int kBarsPerGroup = 2 * R + (kHM ? 2 : 0);  // full, empty, query slots
+  // Head major: query slots per group.  Two let the producer load the next
+  // item's query rows while the consumers still hold the slot of the
+  // current one; above 16 heads one slot, which leaves room for a deeper
+  // ring (the consumers release the slot at an item's first stage).
+  static constexpr int kNQ = kHM ? (GS >= 2 ? 1 : 2) : 0;
+  static constexpr int kQSlots = kGroups * kNQ * T::kQ;
+  static constexpr int kBarsPerGroup = 2 * R + kNQ;  // full, empty, query slots
   static constexpr int kBars = kGroups * kBarsPerGroup * 8;
   static constexpr int kMeta = kGroups * R * static_cast<int>(sizeof(StageMeta));
   static constexpr int kUsed = kRing + kQSlots + kBars + kMeta;  // then the equal-share arrays
@@ -104,11 +109,28 @@ __global__ void __launch_bounds__(NW * 32, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // Equal shares: the first lengths are loaded before anything else (the
+  // prologue's scan waits on them), and the block table is prefetched into
+  // L2, a slice per CTA, for the producers' first block ids after the scan.
+  int ctx_first = 0;
+  if (p.equal_share) {
+    if (static_cast<int>(threadIdx.x) < p.num_seqs) ctx_first = __ldg(p.context_lens + threadIdx.x);
+    const int64_t bytes = static_cast<int64_t>(p.num_seqs) * p.mbs * 4;
+    const int64_t lines = (bytes + 127) / 128;
+    const int64_t per = (lines + gridDim.x - 1) / gridDim.x;
+    for (int64_t i = threadIdx.x; i < per; i += blockDim.x) {
+      const int64_t line = static_cast<int64_t>(blockIdx.x) * per + i;
+      if (line < lines) {
+        const int64_t off = line * 128 < bytes - 4 ? line * 128 : bytes - 4;  // inside the table
+        prefetch_l2(reinterpret_cast<const char*>(p.block_tables) + off);
+      }
+    }
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = warp / S::kWarpsPerGroup, wig = warp % S::kWarpsPerGroup;
   uint8_t* ring = smem + group * R * T::kStage;
-  uint8_t* qslots = smem + S::kRing + group * 2 * T::kQ;  // head major only
+  uint8_t* qslots = smem + S::kRing + group * S::kNQ * T::kQ;  // head major only
   uint64_t* full =
       reinterpret_cast<uint64_t*>(smem + S::kRing + S::kQSlots) + group * S::kBarsPerGroup;
   uint64_t* empty = full + R;
@@ -135,10 +157,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         mbar_init(gb + s, 1);
         mbar_init(gb + R + s, GS);
       }
-      if (kHM) {
-        mbar_init(gb + 2 * R, GS);
-        mbar_init(gb + 2 * R + 1, GS);
-      }
+      for (int i = 0; i < S::kNQ; ++i) mbar_init(gb + 2 * R + i, GS);
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmk);
@@ -173,7 +192,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const int b = base + threadIdx.x;
       int n = 0;
       if (b < p.num_seqs) {
-        int c = __ldg(p.context_lens + b);
+        int c = base == 0 ? ctx_first : __ldg(p.context_lens + b);
         if (c < 0 || c > max_ctx) {  // outside the contract: no keys, flagged
           sk_bad = true;
           c = 0;
@@ -351,8 +370,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     int qslot = 0;
     if (kHM && first) {
       // The slot's previous item must be held in the consumers' registers.
-      qslot = static_cast<int>(q_items & 1);
-      if (q_items >= 2 && !mbar_wait_warp(&qempty[qslot], ((q_items >> 1) - 1) & 1)) {
+      constexpr uint32_t kNQ = S::kNQ > 0 ? S::kNQ : 1;  // (swap AB has no slots)
+      qslot = static_cast<int>(q_items % kNQ);
+      if (q_items >= kNQ && !mbar_wait_warp(&qempty[qslot], ((q_items / kNQ) - 1) & 1)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         p_finished = true;
         return;
@@ -993,9 +1013,15 @@ int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
   // warps plus a producer warp, at most 12 warps per CTA.
   constexpr int kGroups = kHM ? (GS == 1 ? 6 : (GS == 2 ? 4 : 8 / GS)) : 8 / GS;
   constexpr int NW = kGroups * (kHM ? GS + 1 : GS);
-  constexpr int kBudget = (kHM ? 200 : 160) * 1024;  // ring (+ query slots) per CTA
-  constexpr int kR0 = (kBudget / kGroups - (kHM ? 2 * T::kQ : 0)) / T::kStage;
-  constexpr int R = kR0 < 2 ? 2 : (kR0 > 8 ? 8 : kR0);
+  // The ring takes the shared memory left beside the query slots, the
+  // equal-share arrays, barriers and stage records: the deeper each group's
+  // ring, the more bytes in flight per SM (HBM latency under load is a few
+  // microseconds, so in-flight bytes set the streaming rate).
+  constexpr int kNQ = kHM ? (GS >= 2 ? 1 : 2) : 0;
+  constexpr int kFixed = 1024 + static_cast<int>(sk_smem_bytes(kSkMaxSeqs)) +
+                         kGroups * kNQ * T::kQ + 2048;
+  constexpr int kR0 = (227 * 1024 - kFixed) / (kGroups * T::kStage);
+  constexpr int R = kR0 < 2 ? 2 : (kR0 > 12 ? 12 : kR0);
   using S = DecodeSmem<D, GS, NW, R, kHM>;
   static_assert(S::kGroups == kGroups, "warps split into whole groups");
   static_assert(kGroups == decode_groups_per_cta(kHM ? (GS == 1 ? 16 : 16 * GS) : 8),
