@@ -454,95 +454,69 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int i = 0; i < kMT; ++i) qa[i][0] = qa[i][1] = qa[i][2] = qa[i][3] = 0u;
     const int h0 = 16 * wig + g, h1 = h0 + 8;  // this lane's two heads
 
-    // Two stages (32 keys) per iteration while the item goes on: twice the
-    // independent MMA chains between the waits on a stage's copies and on
-    // the row reductions (one stage at a time, the per-tile dependency
-    // chain, not the tensor pipe or HBM, set the pace).  The query rows stay
-    // in registers for the whole item.
     uint32_t c_iter = 0;
     while (true) {
-      const int s0 = static_cast<int>(c_iter % R);
-      if (!mbar_wait_warp(&full[s0], (c_iter / R) & 1)) {
+      const int s = static_cast<int>(c_iter % R);
+      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         break;
       }
-      const StageMeta m0 = meta[s0];
-      if (m0.flags & kDone) break;
-      // a stage that is not its item's last is followed by the same item's
-      // next one, which the producer fills in order
-      const bool pair = !(m0.flags & kLast);
-      const int s1 = static_cast<int>((c_iter + 1) % R);
-      if (pair && !mbar_wait_warp(&full[s1], ((c_iter + 1) / R) & 1)) {
-        if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
-        break;
-      }
-      const StageMeta mL = pair ? meta[s1] : m0;  // the pair's last stage
-      const uint32_t kb0 = smem_u32(ring + s0 * T::kStage), vb0 = kb0 + T::kKV;
-      const uint32_t kb1 = smem_u32(ring + s1 * T::kStage), vb1 = kb1 + T::kKV;
+      const StageMeta m = meta[s];
+      if (m.flags & kDone) break;
+      const uint32_t kbase = smem_u32(ring + s * T::kStage);
+      const uint32_t vbase = kbase + T::kKV;
 
-      if (m0.flags & kFirst) {
+      if (m.flags & kFirst) {
 #pragma unroll
         for (int i = 0; i < kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
         mref[0] = mref[1] = -INFINITY;
         lsum[0] = lsum[1] = 0.f;
         // A operand (Q): this warp's 16 heads, 16-byte chunks along D.
-        const uint32_t qbase = smem_u32(qslots + m0.qslot * T::kQ) + wig * 16 * (D * 2);
+        const uint32_t qbase = smem_u32(qslots + m.qslot * T::kQ) + wig * 16 * (D * 2);
 #pragma unroll
         for (int ks = 0; ks < kMT; ++ks)
           ldsm_x4(qbase + (rr + ((mi & 1) << 3)) * (D * 2) + (2 * ks + (mi >> 1)) * 16, qa[ks]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[m0.qslot]);
+        if (lane == 0) mbar_arrive(&qempty[m.qslot]);
       }
 
-      // S[16 heads][16 keys] per stage = Q K^T: keys 0-7 and 8-15 as two
-      // 8-wide N tiles, even and odd D steps on separate accumulation
-      // chains; the second stage's chains beside the first's.
-      float acc[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      // S[16 heads][16 keys] = Q K^T: keys 0-7 and 8-15 as two 8-wide N
+      // tiles, even and odd D steps on separate accumulation chains.
+      float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sa1[4] = {0.f, 0.f, 0.f, 0.f};
+      float sb0[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < kMT; ++ks) {
-        uint32_t b[4];
-        const uint32_t koff =
-            (ks >> 2) * 2048 + swz128(rr + ((mi >> 1) << 3), ((ks & 3) << 1) + (mi & 1));
-        const int c = ks & 1;
-        ldsm_x4(kb0 + koff, b);  // keys 0-7 (low, high D half), keys 8-15 (low, high)
-        mma_16816<kBF16>(acc[0 + c], qa[ks], b[0], b[1]);
-        mma_16816<kBF16>(acc[2 + c], qa[ks], b[2], b[3]);
-        if (pair) {
-          ldsm_x4(kb1 + koff, b);
-          mma_16816<kBF16>(acc[4 + c], qa[ks], b[0], b[1]);
-          mma_16816<kBF16>(acc[6 + c], qa[ks], b[2], b[3]);
+        uint32_t b[4];  // keys 0-7 (low, high D half), keys 8-15 (low, high)
+        ldsm_x4(kbase + (ks >> 2) * 2048 + swz128(rr + ((mi >> 1) << 3), ((ks & 3) << 1) + (mi & 1)),
+                b);
+        if (ks & 1) {
+          mma_16816<kBF16>(sb0, qa[ks], b[0], b[1]);
+          mma_16816<kBF16>(sb1, qa[ks], b[2], b[3]);
+        } else {
+          mma_16816<kBF16>(sa0, qa[ks], b[0], b[1]);
+          mma_16816<kBF16>(sa1, qa[ks], b[2], b[3]);
         }
       }
-      // x[t][0..1]: head g, keys 8t + 2q4 (+1); x[t][2..3]: head g + 8
-      // (t = 0, 1 the first stage's tiles, 2, 3 the second's).
-      float x[4][4];
+      // x[nt][0..1]: head g, keys 8nt + 2q4 (+1); x[nt][2..3]: head g + 8.
+      float x[2][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        x[0][i] = (acc[0][i] + acc[1][i]) * p.scale_log2;
-        x[1][i] = (acc[2][i] + acc[3][i]) * p.scale_log2;
-        x[2][i] = pair ? (acc[4][i] + acc[5][i]) * p.scale_log2 : -INFINITY;
-        x[3][i] = pair ? (acc[6][i] + acc[7][i]) * p.scale_log2 : -INFINITY;
+        x[0][i] = (sa0[i] + sb0[i]) * p.scale_log2;
+        x[1][i] = (sa1[i] + sb1[i]) * p.scale_log2;
       }
-      // Only an item's last stage holds fewer than 16 keys.
-      const int nv0 = pair ? kKeyTile : m0.nvalid;
-      const int nv1 = pair ? mL.nvalid : 0;
-      if (nv0 < kKeyTile || nv1 < kKeyTile) {
+      const int nv = m.nvalid;
+      if (nv < kKeyTile) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int nv = t < 2 ? nv0 : nv1;
-          const int k0 = (t & 1) * 8 + 2 * q4;
-          if (k0 >= nv) x[t][0] = x[t][2] = -INFINITY;
-          if (k0 + 1 >= nv) x[t][1] = x[t][3] = -INFINITY;
+        for (int nt = 0; nt < 2; ++nt) {
+          const int k0 = nt * 8 + 2 * q4;
+          if (k0 >= nv) x[nt][0] = x[nt][2] = -INFINITY;
+          if (k0 + 1 >= nv) x[nt][1] = x[nt][3] = -INFINITY;
         }
       }
 
-      // Online softmax per head row; the four lanes of a row hold 8 keys each.
-      float mx0 = fmax3f(fmax3f(x[0][0], x[0][1], x[1][0]), fmax3f(x[1][1], x[2][0], x[2][1]),
-                         fmaxf(x[3][0], x[3][1]));
-      float mx1 = fmax3f(fmax3f(x[0][2], x[0][3], x[1][2]), fmax3f(x[1][3], x[2][2], x[2][3]),
-                         fmaxf(x[3][2], x[3][3]));
+      // Online softmax per head row; the four lanes of a row hold 4 keys each.
+      float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
@@ -565,72 +539,44 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
       const float r0 = mref[0] == -INFINITY ? 0.f : mref[0];
       const float r1 = mref[1] == -INFINITY ? 0.f : mref[1];
-      // P in the A-operand layout of the PV MMA, per stage: pa[0]/pa[1]
-      // keys 0-7, pa[2]/pa[3] keys 8-15.
-      uint32_t pa0[4], pa1[4];
-      pa0[0] = pack2<kBF16>(ex2(x[0][0] - r0), ex2(x[0][1] - r0));
-      pa0[1] = pack2<kBF16>(ex2(x[0][2] - r1), ex2(x[0][3] - r1));
-      pa0[2] = pack2<kBF16>(ex2(x[1][0] - r0), ex2(x[1][1] - r0));
-      pa0[3] = pack2<kBF16>(ex2(x[1][2] - r1), ex2(x[1][3] - r1));
-      pa1[0] = pack2<kBF16>(ex2(x[2][0] - r0), ex2(x[2][1] - r0));
-      pa1[1] = pack2<kBF16>(ex2(x[2][2] - r1), ex2(x[2][3] - r1));
-      pa1[2] = pack2<kBF16>(ex2(x[3][0] - r0), ex2(x[3][1] - r0));
-      pa1[3] = pack2<kBF16>(ex2(x[3][2] - r1), ex2(x[3][3] - r1));
+      // P in the A-operand layout of the PV MMA: a0/a1 keys 0-7, a2/a3 keys 8-15.
+      uint32_t pa[4];
+      pa[0] = pack2<kBF16>(ex2(x[0][0] - r0), ex2(x[0][1] - r0));
+      pa[1] = pack2<kBF16>(ex2(x[0][2] - r1), ex2(x[0][3] - r1));
+      pa[2] = pack2<kBF16>(ex2(x[1][0] - r0), ex2(x[1][1] - r0));
+      pa[3] = pack2<kBF16>(ex2(x[1][2] - r1), ex2(x[1][3] - r1));
       {
-        float e0, e1, e2, e3, f0, f1, f2, f3;
-        unpack2<kBF16>(pa0[0], e0, e1);
-        unpack2<kBF16>(pa0[2], e2, e3);
-        unpack2<kBF16>(pa1[0], f0, f1);
-        unpack2<kBF16>(pa1[2], f2, f3);
-        lsum[0] += ((e0 + e1) + (e2 + e3)) + ((f0 + f1) + (f2 + f3));
-        unpack2<kBF16>(pa0[1], e0, e1);
-        unpack2<kBF16>(pa0[3], e2, e3);
-        unpack2<kBF16>(pa1[1], f0, f1);
-        unpack2<kBF16>(pa1[3], f2, f3);
-        lsum[1] += ((e0 + e1) + (e2 + e3)) + ((f0 + f1) + (f2 + f3));
+        float e0, e1, e2, e3;
+        unpack2<kBF16>(pa[0], e0, e1);
+        unpack2<kBF16>(pa[2], e2, e3);
+        lsum[0] += (e0 + e1) + (e2 + e3);
+        unpack2<kBF16>(pa[1], e0, e1);
+        unpack2<kBF16>(pa[3], e2, e3);
+        lsum[1] += (e0 + e1) + (e2 + e3);
       }
 
-      // O[16 heads][D] += P V per stage; V rows past the valid keys are
-      // zeroed (they may hold any bits, and 0 * NaN would reach the sum).
-      const uint32_t vm0_lo = keep_mask(2 * q4 < nv0, 2 * q4 + 1 < nv0);
-      const uint32_t vm0_hi = keep_mask(8 + 2 * q4 < nv0, 9 + 2 * q4 < nv0);
-      const uint32_t vm1_lo = keep_mask(2 * q4 < nv1, 2 * q4 + 1 < nv1);
-      const uint32_t vm1_hi = keep_mask(8 + 2 * q4 < nv1, 9 + 2 * q4 < nv1);
+      // O[16 heads][D] += P V; V rows past the valid keys are zeroed (they
+      // may hold any bits, and 0 * NaN would reach the sum).
+      const uint32_t vm_lo = keep_mask(2 * q4 < nv, 2 * q4 + 1 < nv);
+      const uint32_t vm_hi = keep_mask(8 + 2 * q4 < nv, 9 + 2 * q4 < nv);
 #pragma unroll
       for (int j = 0; j < kMT; ++j) {
-        // columns 16j..16j+7 (keys 0-7, 8-15), then 16j+8..16j+15
-        const uint32_t voff =
-            (j >> 2) * 2048 + swz128(rr + ((mi & 1) << 3), ((j & 3) << 1) + (mi >> 1));
-        uint32_t v[4];
-        ldsm_x4_t(vb0 + voff, v);
-        if (nv0 < kKeyTile) {
-          v[0] &= vm0_lo;
-          v[1] &= vm0_hi;
-          v[2] &= vm0_lo;
-          v[3] &= vm0_hi;
+        uint32_t v[4];  // columns 16j..16j+7 (keys 0-7, 8-15), then 16j+8..16j+15
+        ldsm_x4_t(vbase + (j >> 2) * 2048 + swz128(rr + ((mi & 1) << 3), ((j & 3) << 1) + (mi >> 1)),
+                  v);
+        if (nv < kKeyTile) {
+          v[0] &= vm_lo;
+          v[1] &= vm_hi;
+          v[2] &= vm_lo;
+          v[3] &= vm_hi;
         }
-        mma_16816<kBF16>(o[2 * j], pa0, v[0], v[1]);
-        mma_16816<kBF16>(o[2 * j + 1], pa0, v[2], v[3]);
-        if (pair) {
-          ldsm_x4_t(vb1 + voff, v);
-          if (nv1 < kKeyTile) {
-            v[0] &= vm1_lo;
-            v[1] &= vm1_hi;
-            v[2] &= vm1_lo;
-            v[3] &= vm1_hi;
-          }
-          mma_16816<kBF16>(o[2 * j], pa1, v[0], v[1]);
-          mma_16816<kBF16>(o[2 * j + 1], pa1, v[2], v[3]);
-        }
+        mma_16816<kBF16>(o[2 * j], pa, v[0], v[1]);
+        mma_16816<kBF16>(o[2 * j + 1], pa, v[2], v[3]);
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&empty[s0]);
-        if (pair) mbar_arrive(&empty[s1]);
-      }
+      if (lane == 0) mbar_arrive(&empty[s]);
 
-      if (mL.flags & kLast) {
-        const StageMeta& m = mL;
+      if (m.flags & kLast) {
         float l0 = lsum[0], l1 = lsum[1];
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -672,7 +618,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
           }
         }
       }
-      c_iter += pair ? 2 : 1;
+      ++c_iter;
     }
   } else {
     // ------------------------------------------------ swap AB, G <= 8
