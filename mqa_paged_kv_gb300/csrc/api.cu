@@ -349,7 +349,6 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   dp.context_lens = context_lens;
   dp.num_seqs = num_seqs;
   dp.sk_prefix = nullptr;
-  dp.sk_chunks = 0;
 
   const ProfileScope prof(st);
   int n = 0, r;
@@ -381,7 +380,6 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
     cp.sk_prefix = nullptr;
     cp.num_kv_heads = num_kv_heads;
     cp.sk_groups = 0;
-    cp.sk_chunks = 0;
     if ((r = launch_combine(cp, bf16, head_dim, st)) < 0) return cuda_error();
     n += r;
   }
@@ -534,7 +532,6 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   dp.context_lens = context_lens;
   dp.num_seqs = num_seqs;
   dp.sk_prefix = reinterpret_cast<int32_t*>(ws + L.seq_info);
-  dp.sk_chunks = L.equal_share ? grid * decode_groups_per_cta(G) * decode_chunks_per_group(G) : 0;
 
   const ProfileScope prof(st);
   int n = 0, r;
@@ -556,7 +553,6 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
     cp.sk_prefix = dp.sk_prefix;
     cp.num_kv_heads = num_kv_heads;
     cp.sk_groups = grid * decode_groups_per_cta(G);
-    cp.sk_chunks = dp.sk_chunks;
     r = L.equal_share ? launch_combine_equal_share(cp, bf16, head_dim, st)
                       : launch_combine(cp, bf16, head_dim, st);
     if (r < 0) return cuda_error();

@@ -51,38 +51,6 @@ constexpr int kFirst = 1, kLast = 2, kDone = 4;
 // by more than this many powers of two.
 constexpr float kRefSlack = 8.f;
 
-// The equal-share ranges of a call's T key tiles: static range g < ng (a
-// warp group's share) covers [g * Ts / ng, (g + 1) * Ts / ng) of the first
-// Ts = T - Td tiles (integer shares, the first Ts mod ng one tile more);
-// range ng + k, a chunk of the dynamic tail, covers [Ts + k c, Ts + (k + 1) c)
-// clipped to T.  The decode kernel and the combine derive the same ranges.
-struct SkRanges {
-  int ng, ts, q, r, c, nch, total;
-  __device__ __forceinline__ int start(int ri) const {
-    return ri <= ng ? ri * q + min(ri, r) : ts + (ri - ng) * c;
-  }
-  __device__ __forceinline__ int end(int ri) const {
-    return ri < ng ? start(ri + 1) : min(ts + (ri - ng + 1) * c, total);
-  }
-  __device__ __forceinline__ int range_of(int t) const {
-    if (t >= ts) return ng + (t - ts) / c;
-    return t < r * (q + 1) ? t / (q + 1) : r + (t - r * (q + 1)) / q;
-  }
-};
-
-__device__ __forceinline__ SkRanges sk_ranges(int total, int ng, int chunks) {
-  SkRanges g;
-  g.total = total;
-  g.ng = ng;
-  const int td = chunks > 0 ? total >> kSkTailShift : 0;
-  g.c = chunks > 0 ? max(1, (td + chunks - 1) / chunks) : 1;
-  g.nch = chunks > 0 ? (td + g.c - 1) / g.c : 0;
-  g.ts = total - td;
-  g.q = g.ts / ng;
-  g.r = g.ts - g.q * ng;
-  return g;
-}
-
 template <int D, int GS, bool kHM>
 struct DecodeTile {
   static constexpr int kBoxes = D / 64;        // 64-column TMA boxes per row
@@ -213,8 +181,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // the wait for the preceding kernels.
   int32_t* skP = reinterpret_cast<int32_t*>(smem + S::kUsed);  // [B + 1]
   int32_t* skC = skP + p.num_seqs + 1;                         // [B] lengths
-  int sk_t = 0, sk_end = 0, sk_gstart = 0, sk_gg = 0;  // position, range end / start / index
-  SkRanges sk_rg{};
+  int sk_t = 0, sk_end = 0, sk_gstart = 0, sk_gg = 0;
   bool sk_bad = false;
   if (p.equal_share) {
     int32_t* wsum = skC + p.num_seqs;
@@ -257,10 +224,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     }
     if (threadIdx.x == 0) skP[p.num_seqs] = carry;
     sk_bad = __syncthreads_or(sk_bad) != 0;
-    sk_rg = sk_ranges(Hkv * carry, static_cast<int>(gridDim.x) * S::kGroups, p.sk_chunks);
+    const int total = Hkv * carry;
+    const int ng = static_cast<int>(gridDim.x) * S::kGroups;
     sk_gg = static_cast<int>(blockIdx.x) * S::kGroups + group;
-    sk_gstart = sk_rg.start(sk_gg);
-    sk_end = sk_rg.end(sk_gg);
+    const int q = total / ng, r = total - q * ng;
+    sk_gstart = sk_gg * q + min(sk_gg, r);
+    sk_end = sk_gstart + q + (sk_gg < r ? 1 : 0);
     sk_t = sk_gstart;
   }
   // Sorted list: its length, read once the list is complete (after the wait
@@ -294,16 +263,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       // The next piece of this group's range: the unit holding tile sk_t
       // (the last sequence whose first tile is at or before it; empty
       // sequences share their successor's prefix), cut at the range's end.
-      // At the range's end, the next chunk of the dynamic tail.
       if (sk_t >= sk_end) {
-        if (sk_rg.nch == 0) {
-          nx.state = 4;
-          return;
-        }
-        uint32_t k = 0;
-        if (lane == 0) k = atomicAdd(&p.hdr->decode_grab, 1u);
-        nx.it = k;
-        nx.state = 1;
+        nx.state = 4;
         return;
       }
       int lo = 0, hi = p.num_seqs - 1;
@@ -325,19 +286,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
       nx.rec.part_idx = (sk_t == su && pe == eu) ? -1 : 2 * sk_gg + (sk_t == sk_gstart ? 0 : 1);
       sk_t = pe;
       nx.state = 2;
-      return;
-    }
-    if (nx.state == 1 && p.equal_share) {  // a chunk of the dynamic tail, or none left
-      const int k = static_cast<int>(__shfl_sync(0xffffffffu, nx.it, 0));
-      if (k >= sk_rg.nch) {
-        nx.state = 4;
-        return;
-      }
-      sk_gg = sk_rg.ng + k;
-      sk_gstart = sk_rg.start(sk_gg);
-      sk_end = sk_rg.end(sk_gg);
-      sk_t = sk_gstart;
-      nx.state = 0;
       return;
     }
     if (nx.state == 0) {
@@ -469,7 +417,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // prefill kernel let it start only after its own wait for the list) and
   // reads the list through L2.
   if (p.equal_share) {
-    if (producer && sk_t < sk_end)  // (a chunk of the tail is taken only after the wait)
+    if (producer)
       while (nx.state < 3) advance();
     griddep_wait();
     if (blockIdx.x == 0) {  // the tile prefix, for the combine
@@ -954,11 +902,11 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_kernel(const Combi
 }
 
 // Merge of the equal-share partials.  Unit u = (b, kvh) owns tiles
-// [S_u, E_u) and each range (a group's share or a tail chunk) its own
-// interval; the unit was cut when its first and last tiles lie in
-// different ranges, g_f and g_l.  Each range g in [g_f, g_l] wrote the
-// unit's piece to its first slot (2g) when it opens inside the unit, and
-// to its second (2g + 1) when the unit opens inside it, which only g_f can.  Per head (one
+// [S_u, E_u) and group g the range [start(g), start(g + 1)); the unit was
+// cut when its first and last tiles lie in different groups, g_f and g_l.
+// Each group g in [g_f, g_l] wrote the unit's piece to its first slot (2g)
+// when its range opens inside the unit, and to its second (2g + 1) when
+// the unit opens inside its range, which only g_f's can.  Per head (one
 // warp): M = max_g lse_g, out = sum_g 2^(lse_g - M) o_g / sum_g 2^(lse_g - M),
 // lse in base 2.  Units that were not cut were written by the decode
 // kernel; sequences without keys get zero rows here.
@@ -991,31 +939,30 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_equal_share_kernel
     store(z);
     return;
   }
-  const SkRanges rg = sk_ranges(Hkv * __ldcg(p.sk_prefix + p.num_seqs), p.sk_groups, p.sk_chunks);
+  const int total = Hkv * __ldcg(p.sk_prefix + p.num_seqs);
+  const int ng = p.sk_groups, q = total / ng, r = total - q * ng;
   const int kvh = h / G, hg = h - kvh * G;
   const int su = Hkv * pb + kvh * n, eu = su + n;
-  const int gf = rg.range_of(su), gl = rg.range_of(eu - 1);
+  auto group_of = [&](int t) {
+    return t < r * (q + 1) ? t / (q + 1) : r + (t - r * (q + 1)) / q;
+  };
+  const int gf = group_of(su), gl = group_of(eu - 1);
   if (gf == gl) return;  // one piece: written by the decode kernel
-  const bool f_second = rg.start(gf) < su;
+  const bool f_second = gf * q + min(gf, r) < su;
   const int np = gl - gf + 1;
-  // ranges between gf and gl that hold no tile (static shares of a grid
-  // with more groups than tiles) wrote nothing
-  auto live = [&](int i) { return rg.start(gf + i) < rg.end(gf + i); };
-  auto slot_row = [&](int i) {  // partial row of piece i (range gf + i)
+  auto slot_row = [&](int i) {  // partial row of piece i (group gf + i)
     const int gg = gf + i;
     return static_cast<int64_t>(2 * gg + (i == 0 && f_second ? 1 : 0)) * G + hg;
   };
   float M = -INFINITY;
-  for (int c = lane; c < np; c += 32)
-    if (live(c)) M = fmaxf(M, __ldcg(p.part_lse + slot_row(c)));
+  for (int c = lane; c < np; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot_row(c)));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[kV], W = 0.f;
 #pragma unroll
   for (int i = 0; i < kV; ++i) acc[i] = 0.f;
   for (int c0 = 0; c0 < np; c0 += 32) {
-    const float l =
-        c0 + lane < np && live(c0 + lane) ? __ldcg(p.part_lse + slot_row(c0 + lane)) : -INFINITY;
+    const float l = c0 + lane < np ? __ldcg(p.part_lse + slot_row(c0 + lane)) : -INFINITY;
     const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : ex2(l - M);
     W += w;
     const int cnt = min(32, np - c0);
@@ -1023,7 +970,7 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_equal_share_kernel
       float v[8][kV];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (j0 + j < cnt && live(c0 + j0 + j)) {
+        if (j0 + j < cnt) {
           const float* src = p.part_o + slot_row(c0 + j0 + j) * D + lane * kV;
           if constexpr (kV == 4) {
             const float4 t = __ldcg(reinterpret_cast<const float4*>(src));

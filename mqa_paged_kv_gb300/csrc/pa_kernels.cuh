@@ -33,14 +33,6 @@ constexpr int decode_groups_per_cta(int G) {
   return G <= 8 ? 8 : (G <= 16 ? 6 : (G <= 32 ? 4 : 2));
 }
 
-// Equal shares leave the last eighth of the key tiles to a dynamic tail:
-// chunks handed out one at a time by an atomic counter, so that groups on
-// SMs that stream faster take more of it (per-SM rates differ by a few per
-// cent from run to run).  Chunks per group, from the partial slots they
-// cost (two slots of G rows per chunk): none above 8 heads.
-constexpr int decode_chunks_per_group(int G) { return G <= 2 ? 4 : (G <= 4 ? 3 : (G <= 8 ? 1 : 0)); }
-constexpr int kSkTailShift = 3;  // dynamic tail = total tiles >> 3
-
 // Shared memory of the equal-share prologue: tile prefix [B + 1], lengths
 // [B] and the scan's warp sums.
 constexpr size_t sk_smem_bytes(int num_seqs) {
@@ -152,13 +144,11 @@ inline bool use_equal_share(int num_seqs, int num_kv_heads, int max_blocks_per_s
 
 // Equal-share workspace: header, the tile prefix over sequences [B + 1]
 // (written by the decode kernel for the combine), and two partial slots
-// per range (a warp group's static share or a chunk of the dynamic tail)
-// -- the unit piece at the start of the range and the one at its end --
-// each holding G rows of D fp32 values and G log-sum-exps.
+// per warp group -- the unit piece at the start of its range and the one
+// at its end -- each holding G rows of D fp32 values and G log-sum-exps.
 inline WsLayout equal_share_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
   const int G = num_heads / num_kv_heads;
-  const int64_t slots = 2 * static_cast<int64_t>(kSkMaxCtas) * decode_groups_per_cta(G) *
-                        (1 + decode_chunks_per_group(G));
+  const int64_t slots = 2 * static_cast<int64_t>(kSkMaxCtas) * decode_groups_per_cta(G);
   WsLayout L;
   size_t off = sizeof(WsHeader);
   L.seq_info = off;  // the tile prefix
@@ -221,7 +211,6 @@ struct DecodeParams {
   const int32_t* context_lens;
   int num_seqs;
   int32_t* sk_prefix;
-  int sk_chunks;  // chunks the dynamic tail is cut into, at most (0: none)
   // 1 in a batch with query chunks: launched after the prefill kernel and
   // beside it, on the SMs its CTAs past the prefill share leave (its other
   // CTAs join as prefill CTAs finish): no wait at the start (the work list
@@ -239,7 +228,7 @@ struct CombineParams {
   int num_seqs, num_heads, head_dim;
   // equal share: the tile prefix over sequences and the decode grid's groups
   const int32_t* sk_prefix;
-  int num_kv_heads, sk_groups, sk_chunks;
+  int num_kv_heads, sk_groups;
 };
 
 // A batch with query chunks runs its prefill and decode kernels side by

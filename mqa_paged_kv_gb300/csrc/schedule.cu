@@ -143,12 +143,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(PrepareParams p) {
   griddep_launch_dependents();  // the attention kernel may start its prologue
   if (p.header_only) {
     // Equal-share decode: the decode kernel derives its work from the
-    // lengths itself; only the status word and the tail's chunk counter of
-    // this call start at zero.
-    if (threadIdx.x == 0) {
-      p.hdr->status = 0;
-      p.hdr->decode_grab = 0;  // the dynamic tail's chunk counter
-    }
+    // lengths itself; only the status word of this call starts at zero.
+    if (threadIdx.x == 0) p.hdr->status = 0;
     griddep_wait();
     return;
   }
