@@ -468,6 +468,25 @@ def test_equal_share_under_cta_limits(limit):
     assert g.status() == 0
 
 
+@pytest.mark.parametrize("G,splits", [(4, 0), (16, 0), (32, 0), (64, 0), (32, 3)])
+def test_repeated_decode_calls_give_the_same_bits(G, splits):
+    # the same call on the same grid repeats its arithmetic exactly: a stage
+    # read before its copy landed, a query slot reused too early or a
+    # partial read before it was written would show up as differing bits
+    hkv = 2 if G <= 16 else 1
+    c = W.make_case(f"rep_g{G}", seed=70 + G, dtype=W.BF16, num_heads=G * hkv,
+                    num_kv_heads=hkv, head_dim=128, block_size=16,
+                    context_lens=np.random.default_rng(G).integers(1, 2500, size=24),
+                    query_lens=np.ones(24, np.int64))
+    g = GpuCase(c)
+    g.write_cache()
+    first = bits(g.attention(num_splits=splits))
+    for _ in range(6):
+        assert np.array_equal(bits(g.attention(num_splits=splits)), first)
+    o64, ob, _, _ = oracle.run_case(c)
+    check_attention(first, o64, ob, c.dtype)
+
+
 def test_equal_share_one_sequence_over_every_group():
     # one MQA unit of 32k keys cut into a piece per warp group (more pieces
     # than a warp's 32 lanes in the merge), and one GQA sequence beside a run
