@@ -313,6 +313,20 @@ PA_API void pa_profile_next_call(void* start_event, void* stop_event);
  */
 PA_API void pa_limit_next_call_ctas(int max_ctas);
 
+/*
+ * Limit, in nanoseconds, of each pipeline wait of the decode kernels (of
+ * paged_attn_decode and of the decode rows of the chunked and
+ * cross-attention calls) enqueued after this call, process-wide; 0 restores
+ * the default of 2 s.  A wait that runs out sets PA_DEV_WAIT_TIMEOUT in the
+ * call's status word; the kernel then stops issuing work, waits (with the
+ * fixed 2 s limit) for the copies it still has in flight, and returns, so
+ * the device stays usable and the next call runs normally; the outputs of
+ * the call that timed out are undefined.  The pages define no such call: it
+ * exists so the timeout path can be exercised (a limit of a few
+ * nanoseconds makes waits give up before the first copies land).
+ */
+PA_API void pa_set_pipeline_wait_limit(uint64_t limit_ns);
+
 /* Library version and the number of kernels the last call enqueued. */
 PA_API int pa_version(void);
 PA_API int pa_last_launch_count(void);

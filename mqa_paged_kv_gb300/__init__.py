@@ -75,6 +75,8 @@ _lib.paged_attn_decode_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _F, _I, _I, _
 _lib.paged_attn_decode_noalloc.restype = _I
 _lib.pa_profile_next_call.argtypes = [_P, _P]
 _lib.pa_profile_next_call.restype = None
+_lib.pa_set_pipeline_wait_limit.argtypes = [ctypes.c_uint64]
+_lib.pa_set_pipeline_wait_limit.restype = None
 
 EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_launch_count",
             "pa_last_cuda_error", "pa_last_cuda_error_string", "pa_limit_next_call_ctas",
@@ -83,7 +85,7 @@ EXPORTED = ["pa_profile_next_call", "pa_status_string", "pa_version", "pa_last_l
             "paged_attn_chunked_prefill_workspace_bytes", "paged_attn_chunked_prefill",
             "pa_read_device_status", "paged_attn_decode_noalloc",
             "paged_attn_cross_attention", "gqa_varlen_prefill_workspace_bytes",
-            "gqa_varlen_prefill"]
+            "gqa_varlen_prefill", "pa_set_pipeline_wait_limit"]
 
 
 class PagedAttnError(RuntimeError):
@@ -351,6 +353,12 @@ def pa_read_device_status(workspace: torch.Tensor, clear: bool = False, stream=N
                                     _stream(stream))
     _check(rc, "pa_read_device_status")
     return int(flags.value)
+
+
+def pa_set_pipeline_wait_limit(limit_ns: int) -> None:
+    """Limit of each pipeline wait of the decode kernels enqueued from now
+    on (0 = the default 2 s); see include/paged_attn.h."""
+    _lib.pa_set_pipeline_wait_limit(int(limit_ns))
 
 
 def pa_limit_next_call_ctas(max_ctas: int) -> None:

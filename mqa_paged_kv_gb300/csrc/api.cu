@@ -5,11 +5,21 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pa_kernels.cuh"
 
 namespace pa {
+
+// Pipeline wait limit of the decode kernels; 0 = the default 2 s.
+std::atomic<uint64_t> g_pipeline_wait_ns{0};
+
+uint64_t pipeline_wait_ns() {
+  const uint64_t v = g_pipeline_wait_ns.load(std::memory_order_relaxed);
+  return v ? v : kWaitTimeoutNs;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -349,6 +359,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   dp.context_lens = context_lens;
   dp.num_seqs = num_seqs;
   dp.sk_prefix = nullptr;
+  dp.wait_ns = pipeline_wait_ns();
 
   const ProfileScope prof(st);
   int n = 0, r;
@@ -420,6 +431,10 @@ const char* pa_last_cuda_error_string(void) {
 int pa_last_launch_count(void) { return g_last_launches; }
 
 void pa_limit_next_call_ctas(int max_ctas) { g_next_ctas = max_ctas > 0 ? max_ctas : 0; }
+
+void pa_set_pipeline_wait_limit(uint64_t limit_ns) {
+  g_pipeline_wait_ns.store(limit_ns, std::memory_order_relaxed);
+}
 
 void pa_profile_next_call(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
@@ -532,6 +547,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
   dp.context_lens = context_lens;
   dp.num_seqs = num_seqs;
   dp.sk_prefix = reinterpret_cast<int32_t*>(ws + L.seq_info);
+  dp.wait_ns = pipeline_wait_ns();
 
   const ProfileScope prof(st);
   int n = 0, r;

@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // A swap-AB group of one warp consumes its own copies in order and never
     // runs more than R stages ahead of itself.
     if ((kHM || GS > 1) && p_iter >= static_cast<uint32_t>(R)) {
-      if (!mbar_wait_warp(&empty[s], ((p_iter / R) - 1) & 1)) {
+      if (!mbar_wait_warp(&empty[s], ((p_iter / R) - 1) & 1, p.wait_ns)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         p_finished = true;
         return;
@@ -372,7 +372,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       // The slot's previous item must be held in the consumers' registers.
       constexpr uint32_t kNQ = S::kNQ > 0 ? S::kNQ : 1;  // (swap AB has no slots)
       qslot = static_cast<int>(q_items % kNQ);
-      if (q_items >= kNQ && !mbar_wait_warp(&qempty[qslot], ((q_items / kNQ) - 1) & 1)) {
+      if (q_items >= kNQ &&
+          !mbar_wait_warp(&qempty[qslot], ((q_items / kNQ) - 1) & 1, p.wait_ns)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         p_finished = true;
         return;
@@ -437,8 +438,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // ------------------------------------------------ head major, G > 8
     if (producer) {
       while (!p_finished) issue_stage();
-      // Leave no copy in flight: wait (bounded) for the latest fill of each
-      // slot, so the CTA never exits with TMA writes pending.
+      // Leave no copy in flight: wait for the latest fill of each slot, so
+      // the CTA never exits with TMA writes pending (the fixed 2 s limit,
+      // whatever the pipeline limit: copies land within microseconds).
       for (uint32_t i = p_iter > static_cast<uint32_t>(R) ? p_iter - R : 0u; i < p_iter; ++i)
         if (!mbar_wait_warp(&full[i % R], (i / R) & 1)) break;
       if (p.concurrent) griddep_wait();  // complete after the prefill kernel beside this one
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     uint32_t c_iter = 0;
     while (true) {
       const int s = static_cast<int>(c_iter % R);
-      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
+      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1, p.wait_ns)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         break;
       }
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     uint32_t c_iter = 0;
     while (true) {
       const int s = static_cast<int>(c_iter % R);
-      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1)) {
+      if (!mbar_wait_warp(&full[s], (c_iter / R) & 1, p.wait_ns)) {
         if (lane == 0) Status::raise(status, PA_DEV_WAIT_TIMEOUT);
         break;
       }
@@ -795,8 +797,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
       ++c_iter;
     }
 
-    // Leave no copy in flight: wait (bounded) for stages this group issued but
-    // did not consume, so the CTA never exits with TMA writes pending.
+    // Leave no copy in flight: wait for stages this group issued but did not
+    // consume, so the CTA never exits with TMA writes pending (the fixed 2 s
+    // limit, whatever the pipeline limit).
     if (producer) {
       while (c_iter < p_iter) {
         const int s = static_cast<int>(c_iter % R);

@@ -78,22 +78,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, suspending the thread for at most hint_ns while the
+// phase is incomplete (instead of the system-dependent time).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; gives up after
-// kWaitTimeoutNs and returns false (the caller records the timeout).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// limit_ns (2 s unless the caller passes another limit) and returns false
+// (the caller records the timeout).  A limit below a millisecond (a test
+// of the timeout path) also bounds each suspension by it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
+  if (limit_ns < 1000000ull) {
+    const uint32_t hint = static_cast<uint32_t>(limit_ns);
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_try_wait_hint(bar, parity, hint)) return true;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
 // Warp-uniform form for code where the whole warp waits: the lanes agree on
 // the outcome, so a timeout seen by only some lanes cannot split the warp
 // ahead of warp-synchronous (.aligned) instructions.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               uint64_t limit_ns = kWaitTimeoutNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
 }
 
 // Fetch the line holding `p` into L2 (no register result, no fault model:

@@ -211,6 +211,10 @@ struct DecodeParams {
   const int32_t* context_lens;
   int num_seqs;
   int32_t* sk_prefix;
+  // Limit of each pipeline wait (a stage's copies, a free stage or query
+  // slot).  The bounded drain of copies still in flight before a CTA exits
+  // keeps the fixed 2 s limit, so every copy lands first.
+  uint64_t wait_ns;
   // 1 in a batch with query chunks: launched after the prefill kernel and
   // beside it, on the SMs its CTAs past the prefill share leave (its other
   // CTAs join as prefill CTAs finish): no wait at the start (the work list
@@ -219,6 +223,9 @@ struct DecodeParams {
   // kernel before completing, so what follows sees both kernels' results.
   int concurrent;
 };
+
+// The pipeline wait limit the next decode kernels get (pa_set_pipeline_wait_limit).
+uint64_t pipeline_wait_ns();
 
 struct CombineParams {
   const SeqInfo* seq_info;

@@ -249,7 +249,7 @@ def test_binding_rejects_mismatched_varlen_tensors(lib):
 
 def _declared_params():
     """Parameter kinds of every PA_API prototype in include/paged_attn.h:
-    'ptr' (any pointer or the stream handle), 'int', 'float', 'size_t'."""
+    'ptr' (any pointer or the stream handle), 'int', 'float', 'size_t', 'u64'."""
     with open(os.path.join(ROOT, "include", "paged_attn.h")) as f:
         text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
     out = {}
@@ -261,6 +261,8 @@ def _declared_params():
                 kinds.append("ptr")
             elif "size_t" in p:
                 kinds.append("size_t")
+            elif "uint64_t" in p:
+                kinds.append("u64")
             elif "float" in p:
                 kinds.append("float")
             else:
@@ -284,6 +286,8 @@ def test_binding_argtypes_match_the_header(lib):
                     issubclass(t, ctypes._Pointer)
             elif k == "size_t":
                 ok = t is ctypes.c_size_t
+            elif k == "u64":
+                ok = t is ctypes.c_uint64
             elif k == "float":
                 ok = t is ctypes.c_float
             else:

@@ -322,6 +322,30 @@ def test_bad_lengths_are_flagged():
     assert g.status() & g.pa.PA_DEV_BAD_LENGTHS
 
 
+@pytest.mark.parametrize("hkv", [8, 1])
+def test_pipeline_wait_timeout_is_flagged_and_the_next_call_recovers(hkv):
+    # a wait limit of a nanosecond makes the decode kernel's waits give up
+    # before the first copies land (swap-AB path at 4 heads per KV head,
+    # head-major at 32): the call returns, its status word says so, and with
+    # the default limit back the next call matches the oracle
+    c = W.head_sweep(80 + hkv, num_kv_heads=hkv, batch=8, ctx_len=700)
+    g = GpuCase(c)
+    g.write_cache()
+    g.pa.pa_set_pipeline_wait_limit(1)
+    try:
+        g.attention()
+        torch.cuda.synchronize()
+        flags = g.status()
+    finally:
+        g.pa.pa_set_pipeline_wait_limit(0)
+    assert flags & g.pa.PA_DEV_WAIT_TIMEOUT
+    out = g.attention()
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    o64, ob, _, _ = oracle.run_case(c)
+    check_attention(bits(out), o64, ob, c.dtype)
+
+
 # --------------------------------------------------------------------------
 # cross-attention over a static encoder cache (no causal mask)
 # --------------------------------------------------------------------------
