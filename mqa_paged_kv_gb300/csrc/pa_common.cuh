@@ -78,33 +78,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, suspending the thread for at most hint_ns while the
-// phase is incomplete (instead of the system-dependent time).
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
-                                                   uint32_t hint_ns) {
+// Non-blocking test of the phase with the given parity (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete; gives up after
 // limit_ns (2 s unless the caller passes another limit) and returns false
-// (the caller records the timeout).  A limit below a millisecond (a test
-// of the timeout path) also bounds each suspension by it.
+// (the caller records the timeout).  Below a millisecond (a test of the
+// timeout path) the wait polls without suspending, so that the limit, not
+// the suspension time of try_wait, decides when it gives up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitTimeoutNs) {
   if (limit_ns < 1000000ull) {
-    const uint32_t hint = static_cast<uint32_t>(limit_ns);
-    if (mbar_try_wait_hint(bar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-      if (mbar_try_wait_hint(bar, parity, hint)) return true;
+      if (mbar_test_wait(bar, parity)) return true;
       if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }

@@ -331,6 +331,9 @@ def test_pipeline_wait_timeout_is_flagged_and_the_next_call_recovers(hkv):
     c = W.head_sweep(80 + hkv, num_kv_heads=hkv, batch=8, ctx_len=700)
     g = GpuCase(c)
     g.write_cache()
+    sweep = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB: out of L2
+    g.attention()  # the workspace exists before the timed-out call
+    float(sweep.sum())
     g.pa.pa_set_pipeline_wait_limit(1)
     try:
         g.attention()
