@@ -22,13 +22,11 @@
 //   warps 1-2  MMA issuers, one per tile: S_t = Q_t K^T (M 128, N 64)
 //              into one of two S buffers in tensor memory, O_t += P_t V
 //              with P_t read from tensor memory (O in tensor memory);
-//   warps 4-19 softmax, eight warps per tile, two threads per row (the
-//              row's TMEM lane; one thread for each half of the 64 keys of
-//              a stage): scale, bottom-right causal mask, running max
-//              (the two halves exchange their maxima through shared
-//              memory), P = 2^(x*scale - m) in the element type written to
-//              one of two P buffers in tensor memory, fp32 partial row
-//              sums, and the epilogue O / l (each half writes half of D).
+//   warps 4-11 softmax, four warps per tile, one thread per row (= TMEM
+//              lane): scale, bottom-right causal mask, running max,
+//              P = 2^(x*scale - m) in the element type written over the
+//              first half of its own S buffer in tensor memory, fp32 row
+//              sum, and the epilogue O / l.
 // Tensor memory holds, per tile, one 64-column S buffer, two 32-column P
 // buffers and O_t.  The QK of the next stage may overwrite S as soon as the
 // softmax warps hold the current S in registers, so it runs while they work
@@ -48,10 +46,10 @@ namespace {
 constexpr int kTcRows = 128;              // M of one tile
 constexpr int kTcKeys = 64;               // keys per stage: N of QK, K of PV
 constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per slot; PV K-steps
-constexpr int kTcSoftmaxWarps = 16;
+constexpr int kTcSoftmaxWarps = 8;
 // warp 0 the K producer, warps 1-2 the MMA issuers, warp 3 the V producer;
 // with the softmax warps after them every SM sub-partition (warp % 4) holds
-// one of these four and two softmax warps of each tile.
+// one of these four and one softmax warp of each tile.
 constexpr int kTcVProducerWarp = 3;
 constexpr int kTcFirstSoftmaxWarp = 4;
 constexpr int kTcThreads = (kTcFirstSoftmaxWarp + kTcSoftmaxWarps) * 32;
@@ -70,9 +68,7 @@ enum : int {
   kBarPvDone = kBarPFull + 4,  // [tile][P buffer]
   kBarOFull = kBarPvDone + 4,  // [tile]
   kBarOEmpty = kBarOFull + 2,  // [tile]
-  kBarXchg = kBarOEmpty + 2,   // [tile][quarter][stage parity]: both halves' maxima posted
-  kBarLsum = kBarXchg + 16,    // [tile][quarter]: both halves' row sums posted
-  kBarSlotFull = kBarLsum + 8  // [slot], then [slot] of empties
+  kBarSlotFull = kBarOEmpty + 2  // [slot], then [slot] of empties
 };
 
 template <int D>
@@ -82,18 +78,14 @@ struct TcCfg {
   static constexpr int kQ = kBoxes * kQRegion;       // one Q tile
   static constexpr int kRegion = kTcKeys * 128;      // 64 keys x 128 B
   static constexpr int kSlot = kBoxes * kRegion;     // 64 keys of K or of V
-  static constexpr int kSlots = D == 128 ? 9 : 20;   // ring depth
+  static constexpr int kSlots = D == 128 ? 10 : 20;  // ring depth
   static constexpr int kBarSlotEmpty = kBarSlotFull + kSlots;
   static constexpr int kNumBars = kBarSlotEmpty + kSlots;
   static constexpr int kOffRing = 2 * kQ;
   static constexpr int kOffBar = kOffRing + kSlots * kSlot;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
-  // the two halves of a row exchange maxima [tile][quarter][parity][half][lane]
-  // and row sums [tile][quarter][half][lane] (fp32)
-  static constexpr int kOffXchg = (kOffTmem + 16 + 15) / 16 * 16;
-  static constexpr int kOffLsum = kOffXchg + 2 * 4 * 2 * 2 * 32 * 4;
-  static constexpr int kBytes = kOffLsum + 2 * 4 * 2 * 32 * 4 + 1024;
+  static constexpr int kBytes = kOffTmem + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // Tile t: S (fp32, 64 columns) at t * 128, P buffer pb (16-bit pairs, 32
   // columns) at t * 128 + 64 + 32 * pb; O_t at 256 + t * D.
@@ -129,8 +121,8 @@ __device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity
 
 }  // namespace
 
-// Twenty warps put five on each of the SM's four register files, which caps
-// a thread at 96 registers (a softmax thread holds 32 scores).
+// Twelve warps put three on each of the SM's four register files, which
+// caps a thread at 168 registers.
 template <bool kBF16, int D, bool kVarlen>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -153,17 +145,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the softmax warps after their item's last S, the V producer after the
     // item record
     mbar_init(&bar[kBarQEmpty], 1 + kTcSoftmaxWarps);
-    for (int i = 0; i < 16; ++i) mbar_init(&bar[kBarXchg + i], 2);
-    for (int i = 0; i < 8; ++i) mbar_init(&bar[kBarLsum + i], 2);
     for (int i = 0; i < 4; ++i) {
-      mbar_init(&bar[kBarPFull + i], 8);
+      mbar_init(&bar[kBarPFull + i], 4);
       mbar_init(&bar[kBarPvDone + i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar[kBarSFull + t], 1);
-      mbar_init(&bar[kBarSFree + t], 8);
+      mbar_init(&bar[kBarSFree + t], 4);
       mbar_init(&bar[kBarOFull + t], 1);
-      mbar_init(&bar[kBarOEmpty + t], 8);
+      mbar_init(&bar[kBarOEmpty + t], 4);
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bar[kBarSlotFull + i], 1);
@@ -454,17 +444,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    constexpr int kHalf = kTcKeys / 2;  // keys of a stage per thread
-    constexpr int kDh = D / 2;          // output columns per thread
-    const int t = (warp - kTcFirstSoftmaxWarp) / 8;           // Q tile of this warp
-    const int half = ((warp - kTcFirstSoftmaxWarp) >> 2) & 1;  // keys [32 half, +32) of a stage
+    const int t = (warp - kTcFirstSoftmaxWarp) / 4;  // Q tile of this warp
     const int quarter = warp & 3;    // TMEM lanes 32*quarter ..
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-    float* xchg = reinterpret_cast<float*>(smem + C::kOffXchg) + (t * 4 + quarter) * (2 * 2 * 32);
-    float* lsum = reinterpret_cast<float*>(smem + C::kOffLsum) + (t * 4 + quarter) * (2 * 32);
-    uint64_t* xbar = &bar[kBarXchg + (t * 4 + quarter) * 2];
-    uint64_t* lbar = &bar[kBarLsum + t * 4 + quarter];
     const int rows_used = G * TQ;
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
     int vslot0 = 0, vslot1 = 0;  // V slot read by the PV of the latest stage on P buffer 0 / 1
@@ -478,8 +461,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // causal: the row's absolute position; cross-attention: every key
       const int pos = p.causal ? m.pos0 + tl : m.nkv - 1;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
-      // m_ref is the same in both halves of a row (it moves on the combined
-      // maximum); l is this half's part of the row sum
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
@@ -491,55 +472,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // S_t(j) complete: this tile's QK no longer reads K(j) (one warp per
         // tile releases its slot) and, after the item's last stage, Q.
-        if (lane == 0 && quarter == 0 && half == 0)
+        if (lane == 0 && quarter == 0)
           mbar_arrive(&bar[C::kBarSlotEmpty + (c0 + kpos(j)) % kSlots]);
         if (lane == 0 && j == n - 1) mbar_arrive(&bar[kBarQEmpty]);
         tc_fence_after();
-        float x[kHalf];
-        {
-          uint32_t r[32];
-          tmem_ld32(lane_base + C::col_s(t) + kHalf * half, r);
-#pragma unroll
-          for (int i = 0; i < kHalf; ++i) x[i] = __uint_as_float(r[i]);
-        }
+        float x[kTcKeys];
+        tmem_ld64f(lane_base + C::col_s(t), x);
         // S is in registers: the next QK of this tile may overwrite it.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kBarSFree + t]);
 
-        const int kb = j * kTcKeys + kHalf * half;
-        const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this half
-        if (__any_sync(0xffffffffu, lim < kHalf - 1)) {
+        const int kb = j * kTcKeys;
+        const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this row
+        if (__any_sync(0xffffffffu, lim < kTcKeys - 1)) {
 #pragma unroll
-          for (int i = 0; i < kHalf; ++i)
+          for (int i = 0; i < kTcKeys; ++i)
             if (i > lim) x[i] = -INFINITY;
         }
-        // Half-row max: three-input max on eight independent chains.  (The
+        // Row max: three-input max on eight independent chains.  (The
         // softmax warps' instruction stream, not the tensor pipe, sets the
         // stage time, so the row arithmetic below uses the widest forms:
         // three-input max, and packed two-float FFMA / FADD / FMUL.)
-        static_assert(kHalf == 32, "the max chains cover 32 columns");
+        static_assert(kTcKeys == 64, "the max chains cover 64 columns");
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = fmax3f(x[e], x[e + 8], x[e + 16]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], x[e + 24]);
-        const float mh = fmax3f(fmax3f(mx8[0], mx8[1], mx8[2]), fmax3f(mx8[3], mx8[4], mx8[5]),
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3f(mx8[e], x[e + 24], x[e + 32]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmax3f(mx8[e], x[e + 40], x[e + 48]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], x[e + 56]);
+        const float mx = fmax3f(fmax3f(mx8[0], mx8[1], mx8[2]), fmax3f(mx8[3], mx8[4], mx8[5]),
                                 fmaxf(mx8[6], mx8[7])) *
                          p.scale_log2;
-        // The row max of both halves: post this half's, wait for the other's.
-        xchg[(pb * 2 + half) * 32 + lane] = mh;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&xbar[pb]);
-        if (!warp_wait_or_flag(&xbar[pb], (g >> 1) & 1, status)) {
-          ok = false;
-          break;
-        }
-        const float mx = fmaxf(mh, xchg[(pb * 2 + (half ^ 1)) * 32 + lane]);
         const bool need = m_ref != -INFINITY && mx > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // O_t must hold PV of stage g - 1 before it is rescaled; each half
-          // rescales its half of the columns.
+          // O_t must hold PV of stage g - 1 before it is rescaled.
           if (g >= 1 && !warp_wait_or_flag(&bar[kBarPvDone + 2 * t + ((g - 1) & 1)],
                                            ((g - 1) >> 1) & 1, status)) {
             ok = false;
@@ -549,10 +519,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float alpha = need ? ex2(m_ref - mx) : 1.f;
           const float2 alpha2 = make_float2(alpha, alpha);
 #pragma unroll 1
-          for (int c = 0; c < kDh / 16; ++c) {
+          for (int c = 0; c < D / 16; ++c) {
             uint32_t r[16];
-            const uint32_t addr = lane_base + C::col_o(t) + kDh * half + c * 16;
-            tmem_ld16(addr, r);
+            tmem_ld16(lane_base + C::col_o(t) + c * 16, r);
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               const float2 v = __fmul2_rn(
@@ -560,7 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               r[i] = __float_as_uint(v.x);
               r[i + 1] = __float_as_uint(v.y);
             }
-            tmem_st16(addr, r);
+            tmem_st16(lane_base + C::col_o(t) + c * 16, r);
           }
           if (need) {
             l *= alpha;
@@ -570,12 +539,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (m_ref == -INFINITY) m_ref = mx;
         const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
 
-        // P = 2^(x * scale - m_ref), in place, then this half's row sum,
-        // then its 32 keys into the P buffer (column c holds keys 2c, 2c+1).
+        // P = 2^(x * scale - m_ref), in place, then its row sum, then the P
+        // row into tensor memory over the first half of its S: column c
+        // holds keys 2c, 2c+1 (those S values are already in registers).
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nr2 = make_float2(neg_ref, neg_ref);
 #pragma unroll
-        for (int i = 0; i < kHalf; i += 2) {
+        for (int i = 0; i < kTcKeys; i += 2) {
           const float2 a = __ffma2_rn(make_float2(x[i], x[i + 1]), sc2, nr2);
           x[i] = ex2(a.x);
           x[i + 1] = ex2(a.y);
@@ -584,7 +554,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) rs[k] = make_float2(x[2 * k], x[2 * k + 1]);
 #pragma unroll
-        for (int i = 8; i < kHalf; i += 8)
+        for (int i = 8; i < kTcKeys; i += 8)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             rs[k] = __fadd2_rn(rs[k], make_float2(x[i + 2 * k], x[i + 2 * k + 1]));
@@ -597,17 +567,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0 && quarter == 0 && half == 0)
+          if (lane == 0 && quarter == 0)
             mbar_arrive(&bar[C::kBarSlotEmpty + (pb ? vslot1 : vslot0)]);
           tc_fence_after();
         }
         const int vs = static_cast<int>((c0 + vpos(j, n)) % kSlots);
         if (pb) vslot1 = vs; else vslot0 = vs;
-        {
+#pragma unroll
+        for (int h = 0; h < kTcKeys / 32; ++h) {
           uint32_t w[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) w[c] = pack2<kBF16>(x[2 * c], x[2 * c + 1]);
-          tmem_st16(lane_base + C::col_p(t, pb) + 16 * half, w);
+          for (int c = 0; c < 16; ++c) w[c] = pack2<kBF16>(x[32 * h + 2 * c], x[32 * h + 2 * c + 1]);
+          tmem_st16(lane_base + C::col_p(t, pb) + 16 * h, w);
         }
 
         // Keys past the sequence inside the last loaded box hold
@@ -615,7 +586,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // but 0 * NaN is not).  Each tile's PV waits only for its own
         // softmax warps, so both tiles' warps write the same zeros.
         if (j == n - 1) {
-          const int r0 = m.nkv - j * kTcKeys;
+          const int r0 = m.nkv - kb;
           const int r1 = min(kTcKeys, (r0 + p.box_rows - 1) / p.box_rows * p.box_rows);
           if (r1 > r0) {
             const uint32_t cv = c0 + vpos(j, n);
@@ -627,7 +598,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint8_t* vst = ring + sv * C::kSlot;
             const int per_row = C::kBoxes * 8;  // 16-byte chunks per key row
             const int total = (r1 - r0) * per_row;
-            for (int i = row + 128 * half; i < total; i += 256) {
+            for (int i = row; i < total; i += 128) {
               const int kr = r0 + i / per_row, cc = i % per_row;
               *reinterpret_cast<uint4*>(vst + (cc >> 3) * C::kRegion + kr * 128 + (cc & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
@@ -642,23 +613,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
 
-      // Epilogue: O_t / l for the valid rows, each half its half of D; the
-      // row sum is the two halves' parts.
-      lsum[half * 32 + lane] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(lbar);
-      if (!warp_wait_or_flag(lbar, t_iter & 1, status)) break;
-      const float lt = l + lsum[(half ^ 1) * 32 + lane];
+      // Epilogue: O_t / l for the valid rows.
       if (!warp_wait_or_flag(&bar[kBarOFull + t], t_iter & 1, status)) break;
       tc_fence_after();
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       uint16_t* orow = static_cast<uint16_t*>(p.out) +
                        (static_cast<int64_t>(m.tok0 + tl) * Hq + static_cast<int64_t>(m.kvh) * G +
-                        row % G) * D + kDh * half;
+                        row % G) * D;
 #pragma unroll
-      for (int c = 0; c < kDh / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_base + C::col_o(t) + kDh * half + c * 32, r);
+        tmem_ld32(lane_base + C::col_o(t) + c * 32, r);
         if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
