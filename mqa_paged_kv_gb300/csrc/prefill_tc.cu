@@ -27,11 +27,8 @@
 //              P = 2^(x*scale - m) in the element type written over the
 //              first half of its own S buffer in tensor memory, fp32 row
 //              sum, and the epilogue O / l.
-// Tensor memory holds, per tile, one 64-column S buffer, two 32-column P
-// buffers and O_t.  The QK of the next stage may overwrite S as soon as the
-// softmax warps hold the current S in registers, so it runs while they work
-// on it; P alternates between its two buffers, and a P buffer is rewritten
-// only after the PV two stages back (which read it) has completed.
+// Tensor memory holds two 64-column S buffers per tile and O_0, O_1, so the
+// QK of the next stage runs while the softmax works on the current one.
 // The running max is a reference that only moves when a row max exceeds it
 // by more than 2^8 (then O and l are rescaled in place); between moves P
 // stays below 256, well inside the element type.  Row maxima run over raw
@@ -62,12 +59,11 @@ struct TcMeta {
 enum : int {
   kBarQFull = 0,
   kBarQEmpty,
-  kBarSFull,                   // [tile]: the tile's latest QK has completed
-  kBarSFree = kBarSFull + 2,   // [tile]: its softmax warps hold that S in registers
-  kBarPFull = kBarSFree + 2,   // [tile][P buffer]
-  kBarPvDone = kBarPFull + 4,  // [tile][P buffer]
-  kBarOFull = kBarPvDone + 4,  // [tile]
-  kBarOEmpty = kBarOFull + 2,  // [tile]
+  kBarSFull,                  // [tile][buffer]
+  kBarPFull = kBarSFull + 4,  // [tile][buffer]
+  kBarPvDone = kBarPFull + 4, // [tile][buffer]
+  kBarOFull = kBarPvDone + 4, // [tile]
+  kBarOEmpty = kBarOFull + 2, // [tile]
   kBarSlotFull = kBarOEmpty + 2  // [slot], then [slot] of empties
 };
 
@@ -87,12 +83,9 @@ struct TcCfg {
   static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
   static constexpr int kBytes = kOffTmem + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // Tile t: S (fp32, 64 columns) at t * 128, P buffer pb (16-bit pairs, 32
-  // columns) at t * 128 + 64 + 32 * pb; O_t at 256 + t * D.
-  static constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t * 128); }
-  static constexpr uint32_t col_p(int t, int pb) {
-    return static_cast<uint32_t>(t * 128 + 64 + 32 * pb);
-  }
+  // S buffer b of tile t (fp32, 64 columns) at t * 128 + b * 64, later P
+  // (16-bit pairs) over its first 32 columns; O_t at 256 + t * D.
+  static constexpr uint32_t col_s(int t, int b) { return static_cast<uint32_t>(t * 128 + b * 64); }
   static constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * D); }
 };
 
@@ -146,12 +139,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // item record
     mbar_init(&bar[kBarQEmpty], 1 + kTcSoftmaxWarps);
     for (int i = 0; i < 4; ++i) {
+      mbar_init(&bar[kBarSFull + i], 1);
       mbar_init(&bar[kBarPFull + i], 4);
       mbar_init(&bar[kBarPvDone + i], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bar[kBarSFull + t], 1);
-      mbar_init(&bar[kBarSFree + t], 4);
       mbar_init(&bar[kBarOFull + t], 1);
       mbar_init(&bar[kBarOEmpty + t], 4);
     }
@@ -357,14 +349,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     // One warp per Q tile, so each tile's chain advances on its own while
     // the pipe runs the other tile's groups.  Per tile the QK of stage j + 1
-    // is issued before the PV of stage j, as soon as the softmax warps hold
-    // S(j) in registers, so it runs while they work on stage j.  The warp
-    // waits on the barriers together and elect.sync inside each MMA picks
-    // the issuing lane.  Each group of MMAs is straight-line code on
-    // descriptors prepared up front: the tensor pipe is fed at its full rate
-    // only when no branch or runtime trip count sits between two tcgen05.mma
-    // (measured on this part: a data-independent branch inside the issue
-    // loop halves the rate).
+    // is issued before the PV of stage j, so it runs while the softmax works
+    // on stage j.  The warp waits on the barriers together and elect.sync
+    // inside each MMA picks the issuing lane.  Each group of MMAs is
+    // straight-line code on descriptors prepared up front: the tensor pipe
+    // is fed at its full rate only when no branch or runtime trip count sits
+    // between two tcgen05.mma (measured on this part: a data-independent
+    // branch inside the issue loop halves the rate).  P lives in the S
+    // buffer that the QK two stages later overwrites, and MMAs on different
+    // accumulators are not ordered, so that QK waits for the PV to complete.
     const int t = warp - 1;
     constexpr uint32_t kIdQK = idesc_f16(kTcRows, kTcKeys, kBF16, false, false);
     constexpr uint32_t kIdPV = idesc_f16(kTcRows, D, kBF16, false, true);
@@ -376,52 +369,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t dk = sdesc_sw128(smem_u32(ring), 16, 1024);             // K-major
     const uint64_t dv = sdesc_sw128(smem_u32(ring), C::kRegion, 1024);     // MN-major
     const uint32_t dout = tmem + C::col_o(t);
-    const uint32_t ds = tmem + C::col_s(t);
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
+    int vslot[2] = {0, 0};  // V slot read by the last PV on each S buffer
     bool ok = true;
 
-    // S_t(j) = Q_t K(j)^T once K(j) landed and the softmax warps hold the
-    // previous S of this tile in registers.
+    // S_t(j) = Q_t K(j)^T once K(j) landed and the PV two stages back no
+    // longer reads that S buffer -- nor its V slot, which this warp then
+    // releases (a plain arrival: a second tcgen05.commit right behind
+    // another one costs the issuing warp about 250 cycles on this part).
     auto issue_qk = [&](int j, int n) -> bool {
       const uint32_t g = g0 + j;
+      const int b = static_cast<int>(g & 1);
       const uint32_t ck = c0 + kpos(j);
       const int sk = static_cast<int>(ck % kSlots);
       if (!warp_wait_or_flag(&bar[kBarSlotFull + sk], (ck / kSlots) & 1, status)) return false;
-      if (g >= 1 && !warp_wait_or_flag(&bar[kBarSFree + t], (g - 1) & 1, status)) return false;
+      if (g >= 2) {
+        if (!warp_wait_or_flag(&bar[kBarPvDone + 2 * t + b], ((g >> 1) - 1) & 1, status))
+          return false;
+        if (lane == 0) mbar_arrive(&bar[C::kBarSlotEmpty + (b ? vslot[1] : vslot[0])]);
+      }
       tc_fence_after();
       const uint64_t dks = dk + static_cast<uint64_t>((sk * C::kSlot) >> 4);
+      const uint32_t ds = tmem + C::col_s(t, b);
 #pragma unroll
       for (int ks = 0; ks < kQkSteps; ++ks)
         umma_f16_warp(ds, dq + (((ks >> 2) * C::kQRegion + (ks & 3) * 32) >> 4),
                       dks + (((ks >> 2) * C::kRegion + (ks & 3) * 32) >> 4), kIdQK,
                       ks > 0 ? 1u : 0u);
-      umma_commit_warp(&bar[kBarSFull + t]);
+      umma_commit_warp(&bar[kBarSFull + 2 * t + b]);
       return true;
     };
     // O_t += P_t(j) V(j) once V(j) landed, P_t(j) is written and (first
     // stage) the previous item's epilogue has read O_t.  All four 16-key
     // steps run on every stage: past the sequence P is 0 and the V rows are
     // zero (zero-filled boxes, or zeroed by the softmax warps inside the
-    // last box).  The softmax warps release V(j)'s slot once this PV
-    // completed (they wait for it before reusing its P buffer).
+    // last box).
     auto issue_pv = [&](int j, int n) -> bool {
       const uint32_t g = g0 + j;
-      const int pb = static_cast<int>(g & 1);
+      const int b = static_cast<int>(g & 1);
       const uint32_t cv = c0 + vpos(j, n);
       const int sv = static_cast<int>(cv % kSlots);
       if (!warp_wait_or_flag(&bar[kBarSlotFull + sv], (cv / kSlots) & 1, status) ||
-          !warp_wait_or_flag(&bar[kBarPFull + 2 * t + pb], (g >> 1) & 1, status) ||
+          !warp_wait_or_flag(&bar[kBarPFull + 2 * t + b], (g >> 1) & 1, status) ||
           (j == 0 && t_iter > 0 &&
            !warp_wait_or_flag(&bar[kBarOEmpty + t], (t_iter - 1) & 1, status)))
         return false;
       tc_fence_after();
       const uint64_t dvs = dv + static_cast<uint64_t>((sv * C::kSlot) >> 4);
-      const uint32_t ap = tmem + C::col_p(t, pb);
+      const uint32_t ap = tmem + C::col_s(t, b);
       umma_f16_ts_warp(dout, ap, dvs, kIdPV, j > 0 ? 1u : 0u);
 #pragma unroll
       for (int ks = 1; ks < kTcSub; ++ks)
         umma_f16_ts_warp(dout, ap + ks * 8, dvs + ((ks * 2048) >> 4), kIdPV, 1u);
-      umma_commit_warp(&bar[kBarPvDone + 2 * t + pb]);
+      umma_commit_warp(&bar[kBarPvDone + 2 * t + b]);
+      if (b) vslot[1] = sv; else vslot[0] = sv;
       if (j == n - 1) umma_commit_warp(&bar[kBarOFull + t]);
       return true;
     };
@@ -450,7 +451,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     const int rows_used = G * TQ;
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
-    int vslot0 = 0, vslot1 = 0;  // V slot read by the PV of the latest stage on P buffer 0 / 1
     while (true) {
       if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
       const TcMeta m = *meta;
@@ -465,8 +465,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         const uint32_t g = g0 + j;
-        const int pb = static_cast<int>(g & 1);
-        if (!warp_wait_or_flag(&bar[kBarSFull + t], g & 1, status)) {
+        const int b = static_cast<int>(g & 1);
+        if (!warp_wait_or_flag(&bar[kBarSFull + 2 * t + b], (g >> 1) & 1, status)) {
           ok = false;
           break;
         }
@@ -477,11 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0 && j == n - 1) mbar_arrive(&bar[kBarQEmpty]);
         tc_fence_after();
         float x[kTcKeys];
-        tmem_ld64f(lane_base + C::col_s(t), x);
-        // S is in registers: the next QK of this tile may overwrite it.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarSFree + t]);
+        tmem_ld64f(lane_base + C::col_s(t, b), x);
 
         const int kb = j * kTcKeys;
         const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this row
@@ -560,25 +556,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             rs[k] = __fadd2_rn(rs[k], make_float2(x[i + 2 * k], x[i + 2 * k + 1]));
         const float2 rsum = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
         l += rsum.x + rsum.y;
-        // P buffer pb was last read by the PV of stage g - 2: wait for it to
-        // complete (then that PV's V slot is free too: one release per tile).
-        if (g >= 2) {
-          if (!warp_wait_or_flag(&bar[kBarPvDone + 2 * t + pb], ((g - 2) >> 1) & 1, status)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0 && quarter == 0)
-            mbar_arrive(&bar[C::kBarSlotEmpty + (pb ? vslot1 : vslot0)]);
-          tc_fence_after();
-        }
-        const int vs = static_cast<int>((c0 + vpos(j, n)) % kSlots);
-        if (pb) vslot1 = vs; else vslot0 = vs;
 #pragma unroll
         for (int h = 0; h < kTcKeys / 32; ++h) {
           uint32_t w[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) w[c] = pack2<kBF16>(x[32 * h + 2 * c], x[32 * h + 2 * c + 1]);
-          tmem_st16(lane_base + C::col_p(t, pb) + 16 * h, w);
+          tmem_st16(lane_base + C::col_s(t, b) + 16 * h, w);
         }
 
         // Keys past the sequence inside the last loaded box hold
@@ -609,7 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarPFull + 2 * t + pb]);
+        if (lane == 0) mbar_arrive(&bar[kBarPFull + 2 * t + b]);
       }
       if (!ok) break;
 
