@@ -528,14 +528,22 @@ def decode_roofline(case, kern_s: float) -> dict:
             "traffic_ratio": (traffic / kvb) if traffic else None}
 
 
-def measure_decode(case, device, splits: int, steps: int, warmup: int, flush) -> dict:
+def measure_decode(case, device, splits: int, steps: int, warmup: int, flush,
+                   cpu: bool = False) -> dict:
     """One decode configuration: step time (cache write + attention call),
-    the decode kernel's live time and its HBM roofline."""
+    the decode kernel's live time and its HBM roofline; with cpu, also the
+    oracle on a bounded sample of the same workload (host cores)."""
     st = Step(case, device, splits)
     t, kt, _, _ = time_steps(st, steps, warmup, flush)
     del st
     ms = float(t.mean())
-    return {"kv_bytes": case.kv_bytes(), "ms_per_step": ms,
+    extra = {}
+    if cpu:
+        try:
+            extra["cpu_baseline"] = cpu_baseline(case, target_s=3.0)
+        except Exception as e:  # reported, never required
+            extra["cpu_baseline"] = {"value": None, "error": str(e)[:200]}
+    return {**extra, "kv_bytes": case.kv_bytes(), "ms_per_step": ms,
             "step_gbs": case.kv_bytes() / (ms / 1e3) / 1e9,
             "tokens_per_s": case.total_query_tokens / (ms / 1e3),
             "step_time_stats": step_time_stats(t),
@@ -543,7 +551,8 @@ def measure_decode(case, device, splits: int, steps: int, warmup: int, flush) ->
             "splits": splits or "auto"}
 
 
-def measure_other_decode_configs(seed: int, device, steps: int, warmup: int, flush) -> dict:
+def measure_other_decode_configs(seed: int, device, steps: int, warmup: int, flush,
+                                 cpu: bool = False) -> dict:
     """The other decode configurations of the benchmark, each with its own
     roofline: the tiny GQA decode (a latency figure), the MQA / GQA / MHA
     sweep at 32 query heads (side by side: KV bytes, tokens/s, kernel
@@ -551,7 +560,7 @@ def measure_other_decode_configs(seed: int, device, steps: int, warmup: int, flu
     decode with automatic and fixed split counts."""
     res = {}
     tiny = W.tiny_gqa_decode(seed)
-    r = measure_decode(tiny, device, 0, steps, warmup, flush)
+    r = measure_decode(tiny, device, 0, steps, warmup, flush, cpu)
     r["latency_us"] = r["ms_per_step"] * 1e3
     r["note"] = ("latency-bound: 0.3 MB of KV; the roofline fraction is reported for "
                  "completeness, the step latency is the figure")
@@ -559,13 +568,14 @@ def measure_other_decode_configs(seed: int, device, steps: int, warmup: int, flu
     sweep = {}
     for hkv in (1, 8, 32):
         c = W.head_sweep(seed, num_kv_heads=hkv)
-        sweep[f"kv{hkv}"] = dict(measure_decode(c, device, 0, steps, warmup, flush),
+        sweep[f"kv{hkv}"] = dict(measure_decode(c, device, 0, steps, warmup, flush, cpu),
                                  num_kv_heads=hkv, G=c.num_heads // hkv)
         del c
     res["head_sweep"] = sweep
     lc = W.long_context_decode(seed)
     res["long_context_decode"] = {
-        ("auto" if s == 0 else str(s)): measure_decode(lc, device, s, steps, warmup, flush)
+        ("auto" if s == 0 else str(s)): measure_decode(lc, device, s, steps, warmup, flush,
+                                                       cpu and s == 0)
         for s in (0, 16, 32, 64)}
     return res
 
@@ -826,7 +836,8 @@ def run_ours(args):
         line["secondary"]["varlen_prefill_llama8b"] = measure_varlen(
             args.seed + rank, device, max(5, args.steps // 2), 3, flush)
         line["secondary"].update(measure_other_decode_configs(
-            args.seed + rank, device, sec_steps, sec_warm, flush))
+            args.seed + rank, device, sec_steps, sec_warm, flush,
+            cpu=rank == 0 and world == 1 and not args.no_cpu_baseline))
 
     if rank == 0 and not args.no_cpu_baseline:
         try:
