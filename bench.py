@@ -64,6 +64,9 @@ def parse_args():
                     help="cache block size for llama8b_decode / mixed_prefill_decode "
                          "(the block-size sweep); 16 is the headline configuration")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--host-link", action="store_true",
+                    help="only measure the host<->device copy rate of pinned buffers over a "
+                         "range of sizes (the link the end-to-end figure's copies cross)")
     return ap.parse_args()
 
 
@@ -851,8 +854,44 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def host_link_rates():
+    """One cudaMemcpyAsync per direction between a pinned host buffer and
+    device memory, over sizes around a decode step's inputs and outputs and
+    up to where the rate saturates; median of 20 CUDA-event timings each."""
+    import torch
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    rows = []
+    for mb in (0.5, 2.1, 3.4, 16, 64, 256):
+        n = int(mb * (1 << 20))
+        h = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d = torch.empty(n, dtype=torch.uint8, device=dev)
+        res = {"bytes": n}
+        for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)),
+                         ("d2h", lambda: h.copy_(d, non_blocking=True))):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            ev = []
+            for _ in range(20):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev.append((a, b))
+            torch.cuda.synchronize()
+            ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+            res[name + "_us"] = ms * 1e3
+            res[name + "_gbs"] = n / (ms / 1e3) / 1e9
+        rows.append(res)
+    print(json.dumps({"host_link": rows}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.host_link:
+        host_link_rates()
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
