@@ -64,7 +64,8 @@ enum : int {
   kBarPvDone = kBarPFull + 4, // [tile][buffer]
   kBarOFull = kBarPvDone + 4, // [tile]
   kBarOEmpty = kBarOFull + 2, // [tile]
-  kBarSlotFull = kBarOEmpty + 2  // [slot], then [slot] of empties
+  kBarStaged = kBarOEmpty + 2, // [tile]: the tile's output rows are in shared memory
+  kBarSlotFull = kBarStaged + 2  // [slot], then [slot] of empties
 };
 
 template <int D>
@@ -74,11 +75,15 @@ struct TcCfg {
   static constexpr int kQ = kBoxes * kQRegion;       // one Q tile
   static constexpr int kRegion = kTcKeys * 128;      // 64 keys x 128 B
   static constexpr int kSlot = kBoxes * kRegion;     // 64 keys of K or of V
-  static constexpr int kSlots = D == 128 ? 10 : 20;  // ring depth
+  static constexpr int kSlots = D == 128 ? 6 : 16;   // ring depth
   static constexpr int kBarSlotEmpty = kBarSlotFull + kSlots;
   static constexpr int kNumBars = kBarSlotEmpty + kSlots;
   static constexpr int kOffRing = 2 * kQ;
-  static constexpr int kOffBar = kOffRing + kSlots * kSlot;
+  // Output staging of a tile: 128 rows of D element-type values, 16-byte
+  // chunks XOR-swizzled by row, so the epilogue's global stores coalesce.
+  static constexpr int kStageTile = kTcRows * D * 2;
+  static constexpr int kOffStage = kOffRing + kSlots * kSlot;
+  static constexpr int kOffBar = kOffStage + 2 * kStageTile;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
   static constexpr int kBytes = kOffTmem + 16 + 1024;
@@ -146,6 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar[kBarOFull + t], 1);
       mbar_init(&bar[kBarOEmpty + t], 4);
+      mbar_init(&bar[kBarStaged + t], 4);
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bar[kBarSlotFull + i], 1);
@@ -596,36 +602,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
 
-      // Epilogue: O_t / l for the valid rows.
+      // Epilogue: O_t / l into shared memory (each thread its row), then the
+      // tile's 128 threads copy the valid rows out in 16-byte pieces that
+      // cover whole rows (a warp writes 512 contiguous bytes where heads of
+      // a token are adjacent; a thread writing its own row would touch 32
+      // lines per warp store).
       if (!warp_wait_or_flag(&bar[kBarOFull + t], t_iter & 1, status)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = static_cast<uint16_t*>(p.out) +
-                       (static_cast<int64_t>(m.tok0 + tl) * Hq + static_cast<int64_t>(m.kvh) * G +
-                        row % G) * D;
+      constexpr int kCh = D / 8;  // 16-byte chunks per row
+      uint8_t* stg = smem + C::kOffStage + t * C::kStageTile;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(lane_base + C::col_o(t) + c * 32, r);
-        if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack2<kBF16>(__uint_as_float(r[8 * q + 0]) * inv,
-                               __uint_as_float(r[8 * q + 1]) * inv);
-            o.y = pack2<kBF16>(__uint_as_float(r[8 * q + 2]) * inv,
-                               __uint_as_float(r[8 * q + 3]) * inv);
-            o.z = pack2<kBF16>(__uint_as_float(r[8 * q + 4]) * inv,
-                               __uint_as_float(r[8 * q + 5]) * inv);
-            o.w = pack2<kBF16>(__uint_as_float(r[8 * q + 6]) * inv,
-                               __uint_as_float(r[8 * q + 7]) * inv);
-            reinterpret_cast<uint4*>(orow + c * 32)[q] = o;
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 o;
+          o.x = pack2<kBF16>(__uint_as_float(r[8 * q + 0]) * inv,
+                             __uint_as_float(r[8 * q + 1]) * inv);
+          o.y = pack2<kBF16>(__uint_as_float(r[8 * q + 2]) * inv,
+                             __uint_as_float(r[8 * q + 3]) * inv);
+          o.z = pack2<kBF16>(__uint_as_float(r[8 * q + 4]) * inv,
+                             __uint_as_float(r[8 * q + 5]) * inv);
+          o.w = pack2<kBF16>(__uint_as_float(r[8 * q + 6]) * inv,
+                             __uint_as_float(r[8 * q + 7]) * inv);
+          const int k = c * 4 + q;
+          *reinterpret_cast<uint4*>(stg + row * (D * 2) + ((k ^ (row & (kCh - 1))) << 4)) = o;
         }
       }
+      // O_t is read: the next item's first PV may overwrite it.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kBarOEmpty + t]);
+      if (lane == 0) {
+        mbar_arrive(&bar[kBarOEmpty + t]);
+        mbar_arrive(&bar[kBarStaged + t]);
+      }
+      if (!warp_wait_or_flag(&bar[kBarStaged + t], t_iter & 1, status)) break;
+      {
+        const int ntok_t = min(max(m.ntok - t * TQ, 0), TQ);  // tokens of this tile
+        const int rows_valid = G * ntok_t;
+        uint16_t* obase = static_cast<uint16_t*>(p.out);
+        for (int i = row; i < kTcRows * kCh; i += kTcRows) {
+          const int r = i / kCh, k = i - r * kCh;
+          if (r >= rows_valid) break;  // rows in order: the rest are past the tile's tokens
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(stg + r * (D * 2) + ((k ^ (r & (kCh - 1))) << 4));
+          const int64_t orow = static_cast<int64_t>(m.tok0 + t * TQ + r / G) * Hq +
+                               static_cast<int64_t>(m.kvh) * G + r % G;
+          *reinterpret_cast<uint4*>(obase + orow * D + k * 8) = v;
+        }
+      }
       g0 += n;
       c0 += 2 * n;
       ++t_iter;
