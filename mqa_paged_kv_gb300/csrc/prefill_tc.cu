@@ -455,7 +455,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int quarter = warp & 3;    // TMEM lanes 32*quarter ..
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-    const int rows_used = G * TQ;
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
     while (true) {
       if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
@@ -463,7 +462,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (m.done) break;
       const int tl = t * TQ + row / G;  // token within the pair
-      const bool valid = row < rows_used && tl < m.ntok;
       // causal: the row's absolute position; cross-attention: every key
       const int pos = p.causal ? m.pos0 + tl : m.nkv - 1;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
@@ -640,17 +638,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!warp_wait_or_flag(&bar[kBarStaged + t], t_iter & 1, status)) break;
       {
+        // Thread `row` of the tile copies chunk k = row % kCh of rows
+        // row / kCh, + kStep, + 2 kStep, ...; the row's (token, head) steps
+        // along with it, so the loop needs no division by G.
+        constexpr int kStep = kTcRows / kCh;
         const int ntok_t = min(max(m.ntok - t * TQ, 0), TQ);  // tokens of this tile
         const int rows_valid = G * ntok_t;
-        uint16_t* obase = static_cast<uint16_t*>(p.out);
-        for (int i = row; i < kTcRows * kCh; i += kTcRows) {
-          const int r = i / kCh, k = i - r * kCh;
-          if (r >= rows_valid) break;  // rows in order: the rest are past the tile's tokens
+        const int k = row & (kCh - 1);
+        int r = row / kCh;
+        int tok = r / G, h = r - tok * G;
+        const int dtok = kStep / G, dh = kStep - dtok * G;
+        uint16_t* obase = static_cast<uint16_t*>(p.out) +
+                          (static_cast<int64_t>(m.tok0 + t * TQ) * Hq +
+                           static_cast<int64_t>(m.kvh) * G) * D + k * 8;
+        for (; r < rows_valid; r += kStep) {  // rows in order: the rest are past the tile's tokens
           const uint4 v =
               *reinterpret_cast<const uint4*>(stg + r * (D * 2) + ((k ^ (r & (kCh - 1))) << 4));
-          const int64_t orow = static_cast<int64_t>(m.tok0 + t * TQ + r / G) * Hq +
-                               static_cast<int64_t>(m.kvh) * G + r % G;
-          *reinterpret_cast<uint4*>(obase + orow * D + k * 8) = v;
+          *reinterpret_cast<uint4*>(obase + (static_cast<int64_t>(tok) * Hq + h) * D) = v;
+          tok += dtok;
+          h += dh;
+          if (h >= G) {
+            h -= G;
+            ++tok;
+          }
         }
       }
       g0 += n;
