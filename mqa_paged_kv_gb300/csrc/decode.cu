@@ -68,11 +68,11 @@ struct DecodeSmem {
   static constexpr int kWarpsPerGroup = kHM ? GS + 1 : GS;
   static constexpr int kGroups = NW / kWarpsPerGroup;
   static constexpr int kRing = kGroups * R * T::kStage;
-  // Head major: query slots per group.  Two let the producer load the next
-  // item's query rows while the consumers still hold the slot of the
-  // current one; above 16 heads one slot, which leaves room for a deeper
-  // ring (the consumers release the slot at an item's first stage).
-  static constexpr int kNQ = kHM ? (GS >= 2 ? 1 : 2) : 0;
+  // Head major: two query slots per group, so that the producer can load
+  // the next item's query rows while the consumers still read the slot of
+  // the current one (they release it only at the end of the item's first
+  // stage, once the MMAs that take its fragments have issued).
+  static constexpr int kNQ = kHM ? 2 : 0;
   static constexpr int kQSlots = kGroups * kNQ * T::kQ;
   static constexpr int kBarsPerGroup = 2 * R + kNQ;  // full, empty, query slots
   static constexpr int kBars = kGroups * kBarsPerGroup * 8;
@@ -369,7 +369,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const bool last = key_base + kKeyTile >= cur.key_end;
     int qslot = 0;
     if (kHM && first) {
-      // The slot's previous item must be held in the consumers' registers.
+      // The slot's previous item must be in the consumers' registers (its
+      // first stage is done).
       constexpr uint32_t kNQ = S::kNQ > 0 ? S::kNQ : 1;  // (swap AB has no slots)
       qslot = static_cast<int>(q_items % kNQ);
       if (q_items >= kNQ &&
@@ -478,8 +479,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
         for (int ks = 0; ks < kMT; ++ks)
           ldsm_x4(qbase + (rr + ((mi & 1) << 3)) * (D * 2) + (2 * ks + (mi >> 1)) * 16, qa[ks]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[m.qslot]);
+        // The slot is released with the stage, below: an arrive issued right
+        // after these loads, before any instruction takes their registers,
+        // let the producer's copy of a later item's rows land while a warp
+        // was still reading, and the warp saw a mix of the two items' rows.
       }
 
       // S[16 heads][16 keys] = Q K^T: keys 0-7 and 8-15 as two 8-wide N
@@ -576,7 +579,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
         mma_16816<kBF16>(o[2 * j + 1], pa, v[2], v[3]);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) {
+        // The MMAs above took every K, V and Q fragment of the stage.
+        mbar_arrive(&empty[s]);
+        if (m.flags & kFirst) mbar_arrive(&qempty[m.qslot]);
+      }
 
       if (m.flags & kLast) {
         float l0 = lsum[0], l1 = lsum[1];
@@ -1020,7 +1027,7 @@ int launch_decode_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const Decode
   // equal-share arrays, barriers and stage records: the deeper each group's
   // ring, the more bytes in flight per SM (HBM latency under load is a few
   // microseconds, so in-flight bytes set the streaming rate).
-  constexpr int kNQ = kHM ? (GS >= 2 ? 1 : 2) : 0;
+  constexpr int kNQ = kHM ? 2 : 0;
   constexpr int kFixed = 1024 + static_cast<int>(sk_smem_bytes(kSkMaxSeqs)) +
                          kGroups * kNQ * T::kQ + 2048;
   constexpr int kR0 = (227 * 1024 - kFixed) / (kGroups * T::kStage);
