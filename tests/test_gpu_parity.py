@@ -514,6 +514,33 @@ def test_repeated_decode_calls_give_the_same_bits(G, splits):
     check_attention(first, o64, ob, c.dtype)
 
 
+@pytest.mark.parametrize("G", [16, 32, 64])
+def test_head_major_bits_repeat_between_other_problems(G):
+    # Between calls a GQA decode of 0.7 GB runs, so the next call's keys come
+    # from HBM again and its warps are timed differently.  A query slot handed
+    # back before the warps' reads of it had finished let the next item's
+    # rows into one warp's item in about 7 % of such calls (one sequence,
+    # some heads); 300 calls leave no room for that.
+    hkv = 2 if G == 16 else 1
+    c = W.make_case(f"hm_g{G}", seed=80 + G, dtype=W.BF16, num_heads=G * hkv,
+                    num_kv_heads=hkv, head_dim=128, block_size=16,
+                    context_lens=np.full(40, 700), query_lens=np.ones(40, np.int64))
+    g = GpuCase(c)
+    g.write_cache()
+    other = GpuCase(W.llama8b_decode(21, batch=48, max_ctx=2048))
+    other.write_cache()
+    first = g.attention().clone()
+    torch.cuda.synchronize()
+    o64, ob, _, _ = oracle.run_case(c)
+    check_attention(bits(first), o64, ob, c.dtype)
+    same = 0
+    for _ in range(300):
+        other.attention()
+        same += int(torch.equal(g.attention().view(torch.int16), first.view(torch.int16)))
+    assert same == 300
+    assert g.status() == 0
+
+
 def test_equal_share_one_sequence_over_every_group():
     # one MQA unit of 32k keys cut into a piece per warp group (more pieces
     # than a warp's 32 lanes in the merge), and one GQA sequence beside a run
