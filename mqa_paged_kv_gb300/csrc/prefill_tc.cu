@@ -467,8 +467,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
-      float x[kTcKeys];
-      bool have_s = false;  // x already holds this stage's S (loaded during the last stage)
       for (int j = 0; j < n; ++j) {
         const uint32_t g = g0 + j;
         const int b = static_cast<int>(g & 1);
@@ -482,8 +480,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive(&bar[C::kBarSlotEmpty + (c0 + kpos(j)) % kSlots]);
         if (lane == 0 && j == n - 1) mbar_arrive(&bar[kBarQEmpty]);
         tc_fence_after();
-        if (!have_s) tmem_ld64f(lane_base + C::col_s(t, b), x);
-        have_s = false;
+        float x[kTcKeys];
+        tmem_ld64f(lane_base + C::col_s(t, b), x);
 
         const int kb = j * kTcKeys;
         const int lim = min(pos, m.nkv - 1) - kb;  // last visible column of this row
@@ -563,7 +561,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float2 rsum = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
         l += rsum.x + rsum.y;
 #pragma unroll
-#pragma unroll
         for (int h = 0; h < kTcKeys / 32; ++h) {
           uint32_t w[16];
 #pragma unroll
@@ -596,18 +593,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fence_proxy_async();
           }
         }
-        // When the next stage's S is already complete, load it now: its
-        // latency overlaps that of this stage's P store (x is free: P is in
-        // the store's registers).
-        if (j + 1 < n) {
-          const uint32_t g1 = g + 1;
-          const int b1 = static_cast<int>(g1 & 1);
-          if (__all_sync(0xffffffffu, mbar_test_wait(&bar[kBarSFull + 2 * t + b1], (g1 >> 1) & 1))) {
-            tc_fence_after();
-            tmem_ld64f(lane_base + C::col_s(t, b1), x);
-            have_s = true;
-          }
-        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -625,7 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       constexpr int kCh = D / 8;  // 16-byte chunks per row
       uint8_t* stg = smem + C::kOffStage + t * C::kStageTile;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(lane_base + C::col_o(t) + c * 32, r);
