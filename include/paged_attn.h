@@ -119,8 +119,9 @@ PA_API int reshape_and_cache(const void* k, const void* v, void* k_cache,
 
 /*
  * Workspace size in bytes for paged_attn_decode with these sizes.
- * num_splits: 0 = automatic (splits of 256 tokens, at most 64 per
- * sequence), else the fixed number of KV splits per sequence (1..64).
+ * num_splits: 0 = automatic (equal shares of the batch's key tiles up to
+ * 2048 sequences, else splits of 256 tokens, at most 64 per sequence),
+ * else the fixed number of KV splits per sequence (1..64).
  */
 PA_API size_t paged_attn_workspace_bytes(int num_seqs, int num_heads,
                                   int num_kv_heads, int head_dim,
@@ -132,11 +133,16 @@ PA_API size_t paged_attn_workspace_bytes(int num_seqs, int num_heads,
  *
  *   q [num_seqs, num_heads, head_dim]; out [num_seqs, num_heads, head_dim]
  *
- * Long contexts are cut into KV splits (split s of a sequence with nb
- * blocks covers blocks [s * c, (s + 1) * c), c = ceil(nb / S)); each split
- * gives a partial output and its log-sum-exp, merged by a log-sum-exp
- * combine.  num_splits = 0 picks S per sequence (256-token splits, at most
- * 64).  scale (> 0) multiplies q . k before the softmax (base e).
+ * num_splits = 0 (up to 2048 sequences): the batch's 16-key tiles, over
+ * all (sequence, KV head) units, are shared out in equal contiguous ranges
+ * over the warp groups of a persistent grid; a unit cut between groups
+ * gives one partial output and log-sum-exp per piece, merged by a
+ * log-sum-exp combine kernel.  Larger batches take 256-token splits, at
+ * most 64.
+ * num_splits = S > 0: split s of a sequence with nb blocks covers blocks
+ * [s * c, (s + 1) * c), c = ceil(nb / S), and a combine kernel merges the
+ * splits.  Sequences with no keys get zero output rows.  scale (> 0)
+ * multiplies q . k before the softmax (base e).
  */
 PA_API int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, int max_blocks_per_seq,
