@@ -941,7 +941,10 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_equal_share_kernel
       *reinterpret_cast<uint32_t*>(dst) = packed[0];
     }
   };
-  const int pb = __ldcg(p.sk_prefix + b), n = __ldcg(p.sk_prefix + b + 1) - pb;
+  // The three prefix entries this head needs, loaded together.
+  const int pb = __ldcg(p.sk_prefix + b), pe = __ldcg(p.sk_prefix + b + 1);
+  const int total = Hkv * __ldcg(p.sk_prefix + p.num_seqs);
+  const int n = pe - pb;
   if (n == 0) {  // no keys: a zero row
     float z[kV];
 #pragma unroll
@@ -949,7 +952,6 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_equal_share_kernel
     store(z);
     return;
   }
-  const int total = Hkv * __ldcg(p.sk_prefix + p.num_seqs);
   const int ng = p.sk_groups, q = total / ng, r = total - q * ng;
   const int kvh = h / G, hg = h - kvh * G;
   const int su = Hkv * pb + kvh * n, eu = su + n;
@@ -964,34 +966,51 @@ __global__ void __launch_bounds__(32 * kCombineHeads) combine_equal_share_kernel
     const int gg = gf + i;
     return static_cast<int64_t>(2 * gg + (i == 0 && f_second ? 1 : 0)) * G + hg;
   };
-  float M = -INFINITY;
-  for (int c = lane; c < np; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot_row(c)));
+  // The pieces' log-sum-exps (lane c: piece c) and the first eight pieces'
+  // rows depend only on the prefix: issue them together, one round trip.
+  auto load_row = [&](int i, float (&dst)[kV]) {
+    const float* src = p.part_o + slot_row(i) * D + lane * kV;
+    if constexpr (kV == 4) {
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+      dst[0] = t.x; dst[1] = t.y; dst[2] = t.z; dst[3] = t.w;
+    } else {
+      const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+      dst[0] = t.x; dst[1] = t.y;
+    }
+  };
+  const float l0 = lane < np ? __ldcg(p.part_lse + slot_row(lane)) : -INFINITY;
+  float v[8][kV];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < np) {
+      load_row(j, v[j]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+    }
+  }
+  float M = l0;
+  for (int c = 32 + lane; c < np; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot_row(c)));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[kV], W = 0.f;
 #pragma unroll
   for (int i = 0; i < kV; ++i) acc[i] = 0.f;
   for (int c0 = 0; c0 < np; c0 += 32) {
-    const float l = c0 + lane < np ? __ldcg(p.part_lse + slot_row(c0 + lane)) : -INFINITY;
+    const float l = c0 == 0 ? l0 : (c0 + lane < np ? __ldcg(p.part_lse + slot_row(c0 + lane)) : -INFINITY);
     const float w = (M == -INFINITY || l == -INFINITY) ? 0.f : ex2(l - M);
     W += w;
     const int cnt = min(32, np - c0);
     for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float v[8][kV];
+      if (c0 > 0 || j0 > 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j0 + j < cnt) {
-          const float* src = p.part_o + slot_row(c0 + j0 + j) * D + lane * kV;
-          if constexpr (kV == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+        for (int j = 0; j < 8; ++j) {
+          if (j0 + j < cnt) {
+            load_row(c0 + j0 + j, v[j]);
           } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-            v[j][0] = t.x; v[j][1] = t.y;
-          }
-        } else {
 #pragma unroll
-          for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+            for (int i = 0; i < kV; ++i) v[j][i] = 0.f;
+          }
         }
       }
 #pragma unroll
