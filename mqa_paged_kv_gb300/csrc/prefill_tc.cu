@@ -57,9 +57,9 @@ struct TcMeta {
 };
 
 enum : int {
-  kBarQFull = 0,
-  kBarQEmpty,
-  kBarSFull,                  // [tile][buffer]
+  kBarQFull = 0,                // [buffer]: the item's record and Q tiles are in place
+  kBarBufFree = kBarQFull + 2,  // [buffer]: its record read, its output rows copied out
+  kBarSFull = kBarBufFree + 2,  // [tile][buffer]
   kBarPFull = kBarSFull + 4,  // [tile][buffer]
   kBarPvDone = kBarPFull + 4, // [tile][buffer]
   kBarOFull = kBarPvDone + 4, // [tile]
@@ -81,11 +81,16 @@ struct TcCfg {
   static constexpr int kOffRing = 2 * kQ;
   // Output staging of a tile: 128 rows of D element-type values, 16-byte
   // chunks XOR-swizzled by row, so the epilogue's global stores coalesce.
+  // Two buffers of two Q tiles each take turns: item i loads its Q tiles
+  // into buffer i mod 2 and, once its MMAs are done, stages its output
+  // rows there over them, so the next item's Q tiles load into the other
+  // buffer while item i still runs.
   static constexpr int kStageTile = kTcRows * D * 2;
+  static_assert(kStageTile == kQ, "a tile's output rows fit over its Q tile");
   static constexpr int kOffStage = kOffRing + kSlots * kSlot;
   static constexpr int kOffBar = kOffStage + 2 * kStageTile;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8;
-  static constexpr int kOffTmem = kOffMeta + static_cast<int>(sizeof(TcMeta));
+  static constexpr int kOffTmem = kOffMeta + 2 * static_cast<int>(sizeof(TcMeta));
   static constexpr int kBytes = kOffTmem + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // S buffer b of tile t (fp32, 64 columns) at t * 128 + b * 64, later P
@@ -131,18 +136,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sq = smem;
+  // Q / staging buffer x of the two (each two tiles of kQ bytes).
+  auto qbuf = [&](uint32_t x) -> uint8_t* { return smem + (x ? C::kOffStage : 0); };
   uint8_t* ring = smem + C::kOffRing;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  TcMeta* meta = reinterpret_cast<TcMeta*>(smem + C::kOffMeta);
+  TcMeta* meta = reinterpret_cast<TcMeta*>(smem + C::kOffMeta);  // [buffer]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&bar[kBarQFull], 1);
-    // the softmax warps after their item's last S, the V producer after the
-    // item record
-    mbar_init(&bar[kBarQEmpty], 1 + kTcSoftmaxWarps);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar[kBarQFull + x], 1);
+      // the V producer once it has read the record, the softmax warps once
+      // their output rows are copied out
+      mbar_init(&bar[kBarBufFree + x], 1 + kTcSoftmaxWarps);
+    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
       mbar_init(&bar[kBarPFull + i], 4);
@@ -239,11 +247,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t it = 0;
         if (lane == 0) it = atomicAdd(&p.hdr->prefill_grab, 1u);
         it = __shfl_sync(0xffffffffu, it, 0);
-        if (t_iter > 0 && !warp_wait_or_flag(&bar[kBarQEmpty], (t_iter - 1) & 1, status)) break;
+        // Buffer x last served item t_iter - 2: its record read and its
+        // output rows copied out.
+        const uint32_t x = t_iter & 1;
+        if (t_iter > 1 &&
+            !warp_wait_or_flag(&bar[kBarBufFree + x], ((t_iter >> 1) - 1) & 1, status))
+          break;
         if (it >= num_items) {
           if (lane == 0) {
-            meta->done = 1;
-            mbar_arrive(&bar[kBarQFull]);
+            meta[x].done = 1;
+            mbar_arrive(&bar[kBarQFull + x]);
           }
           break;
         }
@@ -263,21 +276,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m.done = 0;
           m.b = tile.b;
           m.kbase = tile.kbase;
-          *meta = m;
-          mbar_arrive_expect_tx(&bar[kBarQFull],
+          meta[x] = m;
+          mbar_arrive_expect_tx(&bar[kBarQFull + x],
                                 static_cast<uint32_t>(2 * C::kBoxes * 128 * G * TQ));
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_3d(sq + t * C::kQ + bx * C::kQRegion, &tmq, bx * 64, kvh * G,
-                          tile.tok0 + t * TQ, &bar[kBarQFull]);
+              tma_load_3d(qbuf(x) + t * C::kQ + bx * C::kQRegion, &tmq, bx * 64, kvh * G,
+                          tile.tok0 + t * TQ, &bar[kBarQFull + x]);
         }
       } else {
-        if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
-        const TcMeta m = *meta;
+        const uint32_t x = t_iter & 1;
+        if (!warp_wait_or_flag(&bar[kBarQFull + x], (t_iter >> 1) & 1, status)) break;
+        const TcMeta m = meta[x];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kBarQEmpty]);
+        if (lane == 0) mbar_arrive(&bar[kBarBufFree + x]);
         if (m.done) break;
         tb = m.b;
         kvh = m.kvh;
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Adding (byte offset >> 4) to a descriptor moves its start address; the
     // 14-bit field cannot carry because shared-memory offsets stay below
     // 256 KB.
-    const uint64_t dq = sdesc_sw128(smem_u32(sq + t * C::kQ), 16, 1024);
+    uint64_t dq = 0;  // this item's Q tile (its buffer's tile t)
     const uint64_t dk = sdesc_sw128(smem_u32(ring), 16, 1024);             // K-major
     const uint64_t dv = sdesc_sw128(smem_u32(ring), C::kRegion, 1024);     // MN-major
     const uint32_t dout = tmem + C::col_o(t);
@@ -434,11 +448,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
 
     while (ok) {
-      if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
-      const TcMeta m = *meta;
+      const uint32_t x = t_iter & 1;
+      if (!warp_wait_or_flag(&bar[kBarQFull + x], (t_iter >> 1) & 1, status)) break;
+      const TcMeta m = meta[x];
       __syncwarp();
       if (m.done) break;
       const int n = (m.nkv + kTcKeys - 1) / kTcKeys;
+      dq = sdesc_sw128(smem_u32(qbuf(x) + t * C::kQ), 16, 1024);
       tc_fence_after();
       ok = issue_qk(0, n);
       for (int j = 0; j < n && ok; ++j) {
@@ -457,8 +473,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
     while (true) {
-      if (!warp_wait_or_flag(&bar[kBarQFull], t_iter & 1, status)) break;
-      const TcMeta m = *meta;
+      const uint32_t qb = t_iter & 1;  // this item's Q / staging buffer
+      if (!warp_wait_or_flag(&bar[kBarQFull + qb], (t_iter >> 1) & 1, status)) break;
+      const TcMeta m = meta[qb];
       __syncwarp();
       if (m.done) break;
       const int tl = t * TQ + row / G;  // token within the pair
@@ -475,10 +492,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         // S_t(j) complete: this tile's QK no longer reads K(j) (one warp per
-        // tile releases its slot) and, after the item's last stage, Q.
+        // tile releases its slot).
         if (lane == 0 && quarter == 0)
           mbar_arrive(&bar[C::kBarSlotEmpty + (c0 + kpos(j)) % kSlots]);
-        if (lane == 0 && j == n - 1) mbar_arrive(&bar[kBarQEmpty]);
         tc_fence_after();
         float x[kTcKeys];
         tmem_ld64f(lane_base + C::col_s(t, b), x);
@@ -600,7 +616,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
 
-      // Epilogue: O_t / l into shared memory (each thread its row), then the
+      // Epilogue: O_t / l into shared memory over this item's Q tile t (each
+      // thread its row; O_t complete means every MMA of the tile is, so Q_t
+      // is no longer read), then the
       // tile's 128 threads copy the valid rows out in 16-byte pieces that
       // cover whole rows (a warp writes 512 contiguous bytes where heads of
       // a token are adjacent; a thread writing its own row would touch 32
@@ -609,7 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       constexpr int kCh = D / 8;  // 16-byte chunks per row
-      uint8_t* stg = smem + C::kOffStage + t * C::kStageTile;
+      uint8_t* stg = qbuf(qb) + t * C::kStageTile;  // over this item's Q tile t
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -663,6 +681,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      // The buffer may take a later item's Q tiles (TMA writes): order this
+      // thread's shared-memory accesses before the release.
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarBufFree + qb]);
       g0 += n;
       c0 += 2 * n;
       ++t_iter;
