@@ -272,10 +272,14 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   const int G = num_heads / num_kv_heads;
   const int TQ = prefill_tokens_per_tile(G);
   const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
-  CUtensorMap tmk, tmv, tmq;
+  CUtensorMap tmk, tmv, tmq, tmo;
   if ((rc = encode_cache_map(&tmk, k_cache, rows, head_dim)) != PA_OK) return rc;
   if ((rc = encode_cache_map(&tmv, v_cache, rows, head_dim)) != PA_OK) return rc;
   if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
+      PA_OK)
+    return rc;
+  // The output has q's shape: full tiles leave through the same box.
+  if ((rc = encode_query_map(&tmo, out, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
       PA_OK)
     return rc;
   // The prefill kernel gathers K/V in boxes of gcd(block_size, 64) keys: a
@@ -370,7 +374,7 @@ int run_chunked(const void* q, const void* k_cache, const void* v_cache,
   // decode kernel, launched as its dependent, takes those SMs (and more as
   // prefill CTAs finish).
   if (concurrent) {
-    if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
+    if ((r = launch_prefill_tc(tmk_pf, tmv_pf, tmq, tmo, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
                 grid_sms(dev, cta_limit))) < 0)
       return cuda_error();
     n += r;
@@ -651,12 +655,16 @@ int gqa_varlen_prefill(const void* q, const void* k, const void* v, const int32_
 
   const int G = num_heads / num_kv_heads;
   const int TQ = prefill_tokens_per_tile(G);
-  CUtensorMap tmk, tmv, tmq;
+  CUtensorMap tmk, tmv, tmq, tmo;
   if ((rc = encode_varlen_kv_map(&tmk, k, total_key_tokens, num_kv_heads, head_dim)) != PA_OK)
     return rc;
   if ((rc = encode_varlen_kv_map(&tmv, v, total_key_tokens, num_kv_heads, head_dim)) != PA_OK)
     return rc;
   if ((rc = encode_query_map(&tmq, q, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
+      PA_OK)
+    return rc;
+  // The output has q's shape: full tiles leave through the same box.
+  if ((rc = encode_query_map(&tmo, out, total_query_tokens, num_heads, head_dim, G, TQ / 2)) !=
       PA_OK)
     return rc;
 
@@ -705,7 +713,7 @@ int gqa_varlen_prefill(const void* q, const void* k, const void* v, const int32_
   if ((r = launch_prepare(pp, bf16, st)) < 0) return cuda_error();
   n += r;
   prof.begin();
-  if ((r = launch_prefill_tc(tmk, tmv, tmq, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
+  if ((r = launch_prefill_tc(tmk, tmv, tmq, tmo, fp, bf16, head_dim, L.max_tiles * num_kv_heads, st,
                              grid_sms(dev, cta_limit))) < 0)
     return cuda_error();
   n += r;

@@ -287,7 +287,7 @@ int launch_combine_equal_share(const CombineParams& p, bool bf16, int head_dim,
                                cudaStream_t stream);
 
 int launch_prefill_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
-                      const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
+                      const CUtensorMap& tmo, const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
                       cudaStream_t stream, int num_sms);
 
 }  // namespace pa

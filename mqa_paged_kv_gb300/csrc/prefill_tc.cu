@@ -79,8 +79,8 @@ struct TcCfg {
   static constexpr int kBarSlotEmpty = kBarSlotFull + kSlots;
   static constexpr int kNumBars = kBarSlotEmpty + kSlots;
   static constexpr int kOffRing = 2 * kQ;
-  // Output staging of a tile: 128 rows of D element-type values, 16-byte
-  // chunks XOR-swizzled by row, so the epilogue's global stores coalesce.
+  // Output staging of a tile: its 128 rows of D element-type values in the
+  // Q tile's layout, so that one tensor store can take a tile out.
   // Two buffers of two Q tiles each take turns: item i loads its Q tiles
   // into buffer i mod 2 and, once its MMAs are done, stages its output
   // rows there over them, so the next item's Q tiles load into the other
@@ -130,7 +130,8 @@ template <bool kBF16, int D, bool kVarlen>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv,
-                      const __grid_constant__ CUtensorMap tmq, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmq,
+                      const __grid_constant__ CUtensorMap tmo, const PrefillParams p) {
   using C = TcCfg<D>;
   constexpr int kSlots = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -616,18 +617,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
 
-      // Epilogue: O_t / l into shared memory over this item's Q tile t (each
-      // thread its row; O_t complete means every MMA of the tile is, so Q_t
-      // is no longer read), then the
-      // tile's 128 threads copy the valid rows out in 16-byte pieces that
-      // cover whole rows (a warp writes 512 contiguous bytes where heads of
-      // a token are adjacent; a thread writing its own row would touch 32
-      // lines per warp store).
+      // Epilogue: O_t / l into shared memory over this item's Q tile t (O_t
+      // complete means every MMA of the tile is, so Q_t is no longer read),
+      // in the Q tile's own layout: 64-column halves of 128-byte rows, each
+      // row's 16-byte chunks XOR-swizzled by the row as a 128-byte-swizzle
+      // tensor copy places them (each thread writes its row; the swizzle
+      // spreads a warp's stores over all banks).  A tile of full tokens then
+      // leaves in one tensor store per half, issued by one thread; a tile with
+      // fewer tokens (the last of a chunk) is copied out by its 128 threads,
+      // which write only its valid rows.
       if (!warp_wait_or_flag(&bar[kBarOFull + t], t_iter & 1, status)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      constexpr int kCh = D / 8;  // 16-byte chunks per row
-      uint8_t* stg = qbuf(qb) + t * C::kStageTile;  // over this item's Q tile t
+      uint8_t* stg = qbuf(qb) + t * C::kQ;  // over this item's Q tile t
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -643,11 +645,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              __uint_as_float(r[8 * q + 5]) * inv);
           o.w = pack2<kBF16>(__uint_as_float(r[8 * q + 6]) * inv,
                              __uint_as_float(r[8 * q + 7]) * inv);
-          const int k = c * 4 + q;
-          *reinterpret_cast<uint4*>(stg + row * (D * 2) + ((k ^ (row & (kCh - 1))) << 4)) = o;
+          const int k = c * 4 + q;  // chunk of the row: half k / 8, chunk k % 8 of it
+          *reinterpret_cast<uint4*>(stg + (k >> 3) * C::kQRegion + row * 128 +
+                                    (((k & 7) ^ (row & 7)) << 4)) = o;
         }
       }
-      // O_t is read: the next item's first PV may overwrite it.
+      // O_t is read: the next item's first PV may overwrite it.  The rows
+      // go out through the async proxy (a tensor store).
+      fence_proxy_async();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -655,12 +660,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive(&bar[kBarStaged + t]);
       }
       if (!warp_wait_or_flag(&bar[kBarStaged + t], t_iter & 1, status)) break;
-      {
+      const int ntok_t = min(max(m.ntok - t * TQ, 0), TQ);  // tokens of this tile
+      if (ntok_t == TQ) {
+        if (quarter == 0 && lane == 0) {
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_store_3d(&tmo, bx * 64, m.kvh * G, m.tok0 + t * TQ, stg + bx * C::kQRegion);
+          bulk_commit();
+          bulk_wait_read();  // the buffer may be released once the store has read it
+        }
+      } else {
         // Thread `row` of the tile copies chunk k = row % kCh of rows
         // row / kCh, + kStep, + 2 kStep, ...; the row's (token, head) steps
         // along with it, so the loop needs no division by G.
+        constexpr int kCh = D / 8;  // 16-byte chunks per row
         constexpr int kStep = kTcRows / kCh;
-        const int ntok_t = min(max(m.ntok - t * TQ, 0), TQ);  // tokens of this tile
         const int rows_valid = G * ntok_t;
         const int k = row & (kCh - 1);
         int r = row / kCh;
@@ -669,9 +683,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint16_t* obase = static_cast<uint16_t*>(p.out) +
                           (static_cast<int64_t>(m.tok0 + t * TQ) * Hq +
                            static_cast<int64_t>(m.kvh) * G) * D + k * 8;
+        const uint8_t* shalf = stg + (k >> 3) * C::kQRegion;
         for (; r < rows_valid; r += kStep) {  // rows in order: the rest are past the tile's tokens
           const uint4 v =
-              *reinterpret_cast<const uint4*>(stg + r * (D * 2) + ((k ^ (r & (kCh - 1))) << 4));
+              *reinterpret_cast<const uint4*>(shalf + r * 128 + (((k & 7) ^ (r & 7)) << 4));
           *reinterpret_cast<uint4*>(obase + (static_cast<int64_t>(tok) * Hq + h) * D) = v;
           tok += dtok;
           h += dh;
@@ -690,6 +705,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       c0 += 2 * n;
       ++t_iter;
     }
+    // This thread's tensor stores reach global memory before the CTA ends.
+    if (quarter == 0 && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -702,6 +719,7 @@ namespace {
 
 template <bool kBF16, int D, bool kVarlen>
 int launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                        const CUtensorMap& tmo,
                         const PrefillParams& p, int64_t max_items, cudaStream_t stream,
                         int num_sms) {
   using C = TcCfg<D>;
@@ -729,16 +747,17 @@ int launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const CU
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, tmq, p) == cudaSuccess ? 1 : -1;
+  return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, tmq, tmo, p) == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace
 
 int launch_prefill_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmq,
+                      const CUtensorMap& tmo,
                       const PrefillParams& p, bool bf16, int head_dim, int64_t max_items,
                       cudaStream_t stream, int num_sms) {
 #define PA_PREFILL_LAUNCH(B, DIM, V) \
-  launch_prefill_tc_t<B, DIM, V>(tmk, tmv, tmq, p, max_items, stream, num_sms)
+  launch_prefill_tc_t<B, DIM, V>(tmk, tmv, tmq, tmo, p, max_items, stream, num_sms)
   const bool v = p.varlen != 0;
   if (bf16) {
     if (head_dim == 64) return v ? PA_PREFILL_LAUNCH(true, 64, true) : PA_PREFILL_LAUNCH(true, 64, false);
