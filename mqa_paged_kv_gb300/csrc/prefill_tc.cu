@@ -473,6 +473,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     uint32_t t_iter = 0, g0 = 0, c0 = 0;
+    // A tensor store of the previous item's rows that this warp has yet to
+    // see read out of its buffer (then the warp releases that buffer).
+    int pending_buf = -1;
     while (true) {
       const uint32_t qb = t_iter & 1;  // this item's Q / staging buffer
       if (!warp_wait_or_flag(&bar[kBarQFull + qb], (t_iter >> 1) & 1, status)) break;
@@ -614,6 +617,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kBarPFull + 2 * t + b]);
+        if (pending_buf >= 0) {
+          // A stage later the store has long read its rows: release the
+          // previous item's buffer now instead of waiting at its epilogue.
+          if (lane == 0) {
+            bulk_wait_read();
+            mbar_arrive(&bar[kBarBufFree + pending_buf]);
+          }
+          pending_buf = -1;
+        }
       }
       if (!ok) break;
 
@@ -661,14 +673,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!warp_wait_or_flag(&bar[kBarStaged + t], t_iter & 1, status)) break;
       const int ntok_t = min(max(m.ntok - t * TQ, 0), TQ);  // tokens of this tile
+      bool defer = false;  // this warp releases the buffer a stage into the next item
       if (ntok_t == TQ) {
         if (quarter == 0 && lane == 0) {
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_store_3d(&tmo, bx * 64, m.kvh * G, m.tok0 + t * TQ, stg + bx * C::kQRegion);
           bulk_commit();
-          bulk_wait_read();  // the buffer may be released once the store has read it
         }
+        defer = quarter == 0;
       } else {
         // Thread `row` of the tile copies chunk k = row % kCh of rows
         // row / kCh, + kStep, + 2 kStep, ...; the row's (token, head) steps
@@ -700,7 +713,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // thread's shared-memory accesses before the release.
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kBarBufFree + qb]);
+      if (defer)
+        pending_buf = static_cast<int>(qb);
+      else if (lane == 0)
+        mbar_arrive(&bar[kBarBufFree + qb]);
       g0 += n;
       c0 += 2 * n;
       ++t_iter;
