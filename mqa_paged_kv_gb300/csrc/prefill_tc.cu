@@ -559,34 +559,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (m_ref == -INFINITY) m_ref = mx;
         const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
 
-        // P = 2^(x * scale - m_ref), in place, then its row sum, then the P
-        // row into tensor memory over the first half of its S: column c
-        // holds keys 2c, 2c+1 (those S values are already in registers).
+        // P = 2^(x * scale - m_ref), in place, its row sum, and the P row
+        // into tensor memory over the first half of its S (column c holds
+        // keys 2c, 2c+1; those S values are already in registers) -- half by
+        // half, so that the first half's store runs while the second half's
+        // exponentials are computed.  The row sum keeps one accumulation
+        // order, column groups of eight in ascending order.
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nr2 = make_float2(neg_ref, neg_ref);
-#pragma unroll
-        for (int i = 0; i < kTcKeys; i += 2) {
-          const float2 a = __ffma2_rn(make_float2(x[i], x[i + 1]), sc2, nr2);
-          x[i] = ex2(a.x);
-          x[i + 1] = ex2(a.y);
-        }
         float2 rs[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) rs[k] = make_float2(x[2 * k], x[2 * k + 1]);
-#pragma unroll
-        for (int i = 8; i < kTcKeys; i += 8)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            rs[k] = __fadd2_rn(rs[k], make_float2(x[i + 2 * k], x[i + 2 * k + 1]));
-        const float2 rsum = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-        l += rsum.x + rsum.y;
-#pragma unroll
         for (int h = 0; h < kTcKeys / 32; ++h) {
+#pragma unroll
+          for (int i = 32 * h; i < 32 * h + 32; i += 2) {
+            const float2 a = __ffma2_rn(make_float2(x[i], x[i + 1]), sc2, nr2);
+            x[i] = ex2(a.x);
+            x[i + 1] = ex2(a.y);
+          }
+#pragma unroll
+          for (int i = 32 * h; i < 32 * h + 32; i += 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 v = make_float2(x[i + 2 * k], x[i + 2 * k + 1]);
+              rs[k] = i == 0 ? v : __fadd2_rn(rs[k], v);
+            }
+          }
           uint32_t w[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) w[c] = pack2<kBF16>(x[32 * h + 2 * c], x[32 * h + 2 * c + 1]);
           tmem_st16(lane_base + C::col_s(t, b) + 16 * h, w);
         }
+        const float2 rsum = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+        l += rsum.x + rsum.y;
 
         // Keys past the sequence inside the last loaded box hold
         // whatever the cache slots hold: zero those V rows (P is 0 there,
