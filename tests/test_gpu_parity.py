@@ -428,6 +428,30 @@ def test_varlen_prefill_prompts(hq, hkv, D, dtype):
     _run_varlen(c)
 
 
+@pytest.mark.parametrize("G", [3, 12, 48])
+def test_prefill_long_chunks_odd_group_sizes(G):
+    # Long chunks after prefixes: most tiles hold full tokens and leave in
+    # one tensor store whose box is G heads by the tile's tokens (rows
+    # G * TQ < 128 when G does not divide 128); each chunk's last tile is
+    # copied out row by row.  A decode row rides along.
+    hkv = 2 if G <= 12 else 1
+    ql = np.array([300, 1, 257, 190])
+    ctx = ql + np.array([500, 800, 0, 64])
+    c = W.make_case(f"long_g{G}", seed=90 + G, dtype=W.BF16, num_heads=G * hkv,
+                    num_kv_heads=hkv, head_dim=128, block_size=16, context_lens=ctx,
+                    query_lens=ql)
+    run_and_check(c)
+
+
+def test_varlen_prefill_one_token_tiles():
+    # 64 query heads over one KV head: a 128-row tile holds two tokens' 64
+    # heads, so odd prompt lengths end in a one-token tile (copied out row
+    # by row) and every other tile leaves in one tensor store
+    c = W.make_varlen_case("varlen_g64", seed=91, dtype=W.BF16, num_heads=64, num_kv_heads=1,
+                           head_dim=128, q_lens=[1, 70, 129, 256])
+    _run_varlen(c)
+
+
 def test_varlen_prefill_chunks_after_a_prefix():
     # more keys than query rows: the chunk sits at the end (bottom-right)
     c = W.make_varlen_case("varlen_prefix", seed=77, dtype=W.BF16, num_heads=32, num_kv_heads=8,
