@@ -46,10 +46,15 @@ constexpr int kTcSub = kTcKeys / 16;      // 16-key boxes per slot; PV K-steps
 constexpr int kTcSoftmaxWarps = 8;
 // warp 0 the K producer, warps 1-2 the MMA issuers, warp 3 the V producer;
 // with the softmax warps after them every SM sub-partition (warp % 4) holds
-// one of these four and one softmax warp of each tile.
+// one of these four and one softmax warp of each tile.  Warps 12 and 13
+// help the K and V producers: each issues the second half of every slot's
+// boxes when a slot takes four or more (keys gathered in boxes of 16 or 32
+// rows, where the per-warp issue rate of small boxes limits the stage).
 constexpr int kTcVProducerWarp = 3;
 constexpr int kTcFirstSoftmaxWarp = 4;
-constexpr int kTcThreads = (kTcFirstSoftmaxWarp + kTcSoftmaxWarps) * 32;
+constexpr int kTcKHelperWarp = kTcFirstSoftmaxWarp + kTcSoftmaxWarps;
+constexpr int kTcVHelperWarp = kTcKHelperWarp + 1;
+constexpr int kTcThreads = (kTcVHelperWarp + 1) * 32;
 constexpr float kRescaleThreshold = 8.f;  // log2 of the largest unnormalised P
 
 struct TcMeta {
@@ -59,7 +64,8 @@ struct TcMeta {
 enum : int {
   kBarQFull = 0,                // [buffer]: the item's record and Q tiles are in place
   kBarBufFree = kBarQFull + 2,  // [buffer]: its record read, its output rows copied out
-  kBarSFull = kBarBufFree + 2,  // [tile][buffer]
+  kBarMetaFull = kBarBufFree + 2,  // [buffer]: the item's record is written
+  kBarSFull = kBarMetaFull + 2,  // [tile][buffer]
   kBarPFull = kBarSFull + 4,  // [tile][buffer]
   kBarPvDone = kBarPFull + 4, // [tile][buffer]
   kBarOFull = kBarPvDone + 4, // [tile]
@@ -124,10 +130,11 @@ __device__ __forceinline__ bool warp_wait_or_flag(uint64_t* bar, uint32_t parity
 
 }  // namespace
 
-// Twelve warps put three on each of the SM's four register files, which
-// caps a thread at 168 registers.
+// Fourteen warps at 120 registers a thread (no spills) hold 53.8 K of the
+// SM's 64 K registers, so that a CTA fits beside one CTA of the cache write
+// it follows and becomes resident while that kernel still runs.
 template <bool kBF16, int D, bool kVarlen>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(120)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv,
                       const __grid_constant__ CUtensorMap tmq,
@@ -148,9 +155,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar[kBarQFull + x], 1);
-      // the V producer once it has read the record, the softmax warps once
-      // their output rows are copied out
-      mbar_init(&bar[kBarBufFree + x], 1 + kTcSoftmaxWarps);
+      mbar_init(&bar[kBarMetaFull + x], 1);
+      // the V producer and the two helpers once they have read the record,
+      // the softmax warps once their output rows are copied out
+      mbar_init(&bar[kBarBufFree + x], 3 + kTcSoftmaxWarps);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bar[kBarSFull + i], 1);
@@ -191,16 +199,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* status = &p.hdr->status;
   const uint32_t num_items = p.hdr->prefill_items;
 
-  if (warp == 0 || warp == kTcVProducerWarp) {
+  if (warp == 0 || warp == kTcVProducerWarp || warp >= kTcKHelperWarp) {
     // ------------------------------------------------------------ producers
-    // Two warps issue the K/V copies (measured on this part: L2-resident
+    // Four warps issue the K/V copies (measured on this part: L2-resident
     // 2 KB boxes arrive about 1.5x faster from two issuing warps than from
-    // one).  The K warp grabs the work items, publishes each item's record
-    // and loads its Q tiles; the V warp reads the record once Q has landed.
-    // Each fills its own positions of the one ring, whose order
+    // one): a K pair and a V pair, the second warp of a pair issuing the
+    // second half of each slot's boxes onto the same barrier (the first arms
+    // its byte count).  The K warp grabs the work items, publishes each
+    // item's record and loads its Q tiles; the other three read the record.
+    // Each pair fills its own positions of the one ring, whose order
     // K0, K1, V0, K2, V1, ... is the MMAs' consumption order.
-    const bool is_v = warp == kTcVProducerWarp;
-    if (lane == 0 && !is_v) {
+    const bool is_v = warp == kTcVProducerWarp || warp == kTcVHelperWarp;
+    const bool helper = warp >= kTcKHelperWarp;
+    const bool leader = warp == 0;
+    if (lane == 0 && leader) {
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       tma_prefetch_desc(&tmq);
@@ -212,7 +224,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int box_rows = p.box_rows;               // 16, 32 or 64
     const int kboxes = kTcKeys / box_rows;         // boxes per 64 columns
     const int nb = kboxes * C::kBoxes;             // boxes per slot (<= 8)
-    const bool boxer = lane < nb;
+    // With four or more boxes a slot the pair splits them; with fewer the
+    // first warp issues them all and the helper issues nothing.
+    const bool split = nb >= 4;
+    const int nb_first = split ? nb / 2 : nb;  // the first warp's share
+    const bool boxer = helper ? (split && lane >= nb_first && lane < nb) : lane < nb_first;
     const int my_j = lane / C::kBoxes, my_bx = lane % C::kBoxes;
     uint32_t t_iter = 0, c0 = 0;  // c0: ring position of the item's first load
     int cur_kvh = 0;              // KV head of the current item (contiguous K/V)
@@ -227,7 +243,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (q >= static_cast<uint32_t>(kSlots) &&
           !warp_wait_or_flag(&bar[C::kBarSlotEmpty + s], ((q / kSlots) - 1) & 1, status))
         return false;
-      if (lane == 0) mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
+      // The pair's boxes may land before the count is armed: the phase
+      // cannot complete while its one arrival is pending.
+      if (lane == 0 && !helper)
+        mbar_arrive_expect_tx(&bar[kBarSlotFull + s], static_cast<uint32_t>(C::kSlot));
       __syncwarp();
       if constexpr (kVarlen) {  // 64 consecutive tokens of one KV head; row = token
         if (boxer)
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     while (ok) {
       int tb, kvh, nkv, kbase;
-      if (!is_v) {
+      if (leader) {
         uint32_t it = 0;
         if (lane == 0) it = atomicAdd(&p.hdr->prefill_grab, 1u);
         it = __shfl_sync(0xffffffffu, it, 0);
@@ -257,6 +276,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (it >= num_items) {
           if (lane == 0) {
             meta[x].done = 1;
+            mbar_arrive(&bar[kBarMetaFull + x]);
             mbar_arrive(&bar[kBarQFull + x]);
           }
           break;
@@ -278,6 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m.b = tile.b;
           m.kbase = tile.kbase;
           meta[x] = m;
+          mbar_arrive(&bar[kBarMetaFull + x]);  // the other producers start on the record
           mbar_arrive_expect_tx(&bar[kBarQFull + x],
                                 static_cast<uint32_t>(2 * C::kBoxes * 128 * G * TQ));
 #pragma unroll
@@ -289,7 +310,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       } else {
         const uint32_t x = t_iter & 1;
-        if (!warp_wait_or_flag(&bar[kBarQFull + x], (t_iter >> 1) & 1, status)) break;
+        if (!warp_wait_or_flag(&bar[kBarMetaFull + x], (t_iter >> 1) & 1, status)) break;
         const TcMeta m = meta[x];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kBarBufFree + x]);
@@ -346,7 +367,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // read the next sequence's rows (or zeros past the tensor), which the
       // mask and the V-row zeroing cover.
       const int n = (nkv + kTcKeys - 1) / kTcKeys;
-      for (int j = 0; j < n && ok; ++j) {
+      // With fewer than four boxes a slot (64-key boxes) the helpers issue
+      // nothing: they only keep pace with the records.
+      const bool loads = !helper || split;
+      for (int j = 0; j < n && ok && loads; ++j) {
         int row;
         if constexpr (kVarlen)
           row = kbase + j * kTcKeys;

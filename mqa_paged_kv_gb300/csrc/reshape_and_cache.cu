@@ -49,7 +49,10 @@ int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* 
   if (total == 0) return 0;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  // One wave at most (8 CTAs of 256 threads an SM, grid-stride beyond): the
+  // attention kernels launched behind this one become resident as its CTAs
+  // retire, and a second wave would then find the SMs taken.
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
