@@ -242,12 +242,12 @@ struct CombineParams {
 // side, the SMs split by the work-list kernel in proportion to the two
 // kernels' estimated times at these per-SM rates (measured on this part:
 // the decode kernel streams about 6.2 TB/s over 152 SMs, the prefill kernel
-// about 850 TFLOP/s), the decode share shaded down: decode CTAs that find
+// about 940 TFLOP/s), the decode share shaded down: decode CTAs that find
 // no SM at first take over the prefill kernel's SMs as its CTAs finish, so
 // the decode kernel can grow into a misjudged split and the prefill kernel
 // cannot.
 constexpr double kDecodeBytesPerSmSec = 41e9;
-constexpr double kPrefillFlopsPerSmSec = 5.6e12;
+constexpr double kPrefillFlopsPerSmSec = 6.2e12;
 constexpr double kDecodeShareMargin = 0.9;
 
 struct PrefillParams {
