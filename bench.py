@@ -55,7 +55,9 @@ def parse_args():
                     choices=["llama8b_decode", "mixed_prefill_decode", "head_sweep_kv1",
                              "head_sweep_kv8", "head_sweep_kv32", "long_context_decode",
                              "tiny_gqa_decode", "cross_attention_decode",
-                             "cross_attention_prefill"])
+                             "cross_attention_prefill", "varlen_prefill_llama8b"],
+                    help="varlen_prefill_llama8b times gqa_varlen_prefill alone (one GPU; "
+                         "its prefill kernel's tensor roofline), for profiling that kernel")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the mixed-batch line item")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -653,7 +655,34 @@ def measure_varlen(seed: int, device, steps: int, warmup: int, flush):
             "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": ach,
                          "peak": peak, "peak_source": src, "unit": "TFLOP/s",
                          "frac": ach / peak, "kernel_ms": kt * 1e3, "algorithmic_flops": flops,
-                         "traffic": None}}
+                         "traffic": ncu_traffic("prefill_tc_kernel", "prefill_tc.cu",
+                                                "varlen_prefill_llama8b")}}
+
+
+def run_varlen_only(args):
+    """The varlen prompt batch alone on one GPU: its call and prefill-kernel
+    times and the kernel's tensor roofline, as one JSON line."""
+    import torch
+    _, world, _ = dist_env()
+    if world > 1 or args.impl == "reference":
+        raise SystemExit("varlen_prefill_llama8b runs on one GPU with --impl ours only")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    import mqa_paged_kv_gb300  # noqa: F401  (fails loudly when the library is missing)
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    res = measure_varlen(args.seed, device, args.steps, max(3, args.warmup), flush)
+    clocks = clk.stop()
+    r = res["roofline"]
+    print(json.dumps({
+        "metric": "varlen prompt prefill attention TFLOP/s", "value": r["achieved"],
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "varlen_prefill_llama8b", "query_tokens": res["query_tokens"],
+                   "l2": "flushed before every timed call (256 MiB read sweep)"},
+        "tokens_per_s": res["tokens_per_s"], "roofline": r, "clocks": clocks}), flush=True)
 
 
 def measure_two_kernel(seed: int, device, steps: int, warmup: int, flush, block_size: int = 16):
@@ -892,7 +921,9 @@ def main():
     if args.host_link:
         host_link_rates()
         return
-    if args.impl == "reference":
+    if args.workload == "varlen_prefill_llama8b":
+        run_varlen_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
