@@ -38,6 +38,10 @@
  * never create streams.  Scratch space comes from the caller's `workspace`
  * (size from the matching *_workspace_bytes function, 256-byte aligned).
  * Two calls that share a workspace must not run concurrently.
+ * Stream capture: every kernel reads lengths, tables and offsets from device
+ * memory when it runs, so a step captured in a CUDA graph replays correctly
+ * for any batch of the captured shapes (the scalar arguments are baked into
+ * the graph).  Make the first call on a device outside any capture.
  *
  * Errors.  Arguments are validated on the host first; a negative pa_status
  * is returned and nothing is enqueued.  A failed launch returns
