@@ -605,6 +605,55 @@ def prefill_roofline(workload: str, seed: int, device, args, flush):
             "timed_on": f"the {pcase.num_seqs} query chunks of {workload} (seed {seed}) alone"}
 
 
+def graph_replay_times(step, steps: int, warmup: int, flush):
+    """The step (cache write + attention call) captured once in a CUDA graph
+    on a side stream and replayed: CUDA-event time of each replay (ms), L2
+    swept before each, outside the timed interval."""
+    torch = step.torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # the first calls set kernel attributes: not in a capture
+        step.run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step.run()
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        flush.sum()
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    hold_gpu(torch, min(0.5, steps * 3e-4 + 2e-3))
+    for a, b in ev:
+        flush.sum()
+        a.record()
+        graph.replay()
+        b.record()
+    torch.cuda.synchronize()
+    del graph
+    return np.array([a.elapsed_time(b) for a, b in ev])
+
+
+def measure_graph_steps(seed: int, device, steps: int, warmup: int, flush) -> dict:
+    """Decode steps replayed from a CUDA graph (the way a serving loop issues
+    a fixed-shape step): the headline batch and the latency-bound tiny one."""
+    res = {}
+    for name in ("llama8b_decode", "tiny_gqa_decode"):
+        case = make_workload(name, seed)
+        step = Step(case, device, 0)
+        t = graph_replay_times(step, steps, warmup, flush)
+        del step
+        ms = float(t.mean())
+        res[name] = {"ms_per_step": ms, "median_ms": float(np.median(t)),
+                     "step_gbs": case.kv_bytes() / (ms / 1e3) / 1e9,
+                     "tokens_per_s": case.total_query_tokens / (ms / 1e3)}
+    res["note"] = ("cache write + decode call captured once in a CUDA graph and replayed; "
+                   "CUDA events around each replay, L2 swept before each")
+    return res
+
+
 def measure_varlen(seed: int, device, steps: int, warmup: int, flush):
     """gqa_varlen_prefill on the Llama-3.1-8B prompt batch (16 prompts of
     U[128, 2048] tokens, contiguous K/V, no cache): CUDA-event time of the
@@ -870,6 +919,8 @@ def run_ours(args):
         line["secondary"].update(measure_other_decode_configs(
             args.seed + rank, device, sec_steps, sec_warm, flush,
             cpu=rank == 0 and world == 1 and not args.no_cpu_baseline))
+        line["secondary"]["graph_replay"] = measure_graph_steps(
+            args.seed + rank, device, sec_steps, sec_warm, flush)
 
     if rank == 0 and not args.no_cpu_baseline:
         try:
